@@ -1,0 +1,181 @@
+/*
+ * nrc -- normalization-fused, channel-mixing Conv1d blocks on one GB300 (sm_103a).
+ *
+ * C ABI of libnrc.so.  Three blocks, each stated on a PopcornBench page as a
+ * composition of PyTorch modules:
+ *
+ *   nrc_prenorm_dilconv_residual   "Kimi-K2.6 l2_p12", problem statement:
+ *       out = x + Conv1d(ReLU(BatchNorm1d_eval(x))), kernel_size 3,
+ *       padding = dilation (so the output length equals L), C_in = C_out.
+ *   nrc_conv1d_groupnorm           "FW-GLM-5-1 l2_p35", problem analysis:
+ *       Conv1d(C_in -> C_out, kernel_size 3, stride 1, padding 1, dilation 1,
+ *       bias optional) followed by GroupNorm(num_groups, C_out, eps, affine).
+ *   nrc_linear_bn_swish            "Kimi-K2.6 l2_p97", problem statement:
+ *       Linear(in, out) -> BatchNorm1d(out) (training: batch statistics and
+ *       running-stat update; eval: running statistics) -> + scalar bias ->
+ *       / divide_value -> x * sigmoid(x).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is a DEVICE pointer to caller-owned, contiguous
+ *   memory in PyTorch's default layout: activations (N, C, L) with L fastest,
+ *   conv weights (C_out, C_in, 3) with the tap index fastest, Linear weights
+ *   (out_features, in_features) with in_features fastest.
+ * - The library never allocates.  Scratch space is the caller's `workspace`
+ *   (device memory, 256-byte aligned, at least *_workspace_size() bytes).
+ * - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *   is the legacy default stream).  No call synchronises the host.  The
+ *   workspace and outputs must not be reused until the stream has passed the
+ *   call.
+ * - Argument errors are reported by the return value before anything is
+ *   launched; a failed launch returns NRC_ERR_CUDA.  A device-side wait that
+ *   gives up (see nrc_set_wait_timeout_ns) is recorded in the device status
+ *   word and reported by nrc_query_status().  No call throws or aborts.
+ * - Arithmetic: fp32 storage is computed with three bf16 tensor-core products
+ *   per term (hi*hi + lo*hi + hi*lo with v = hi + lo), accumulated in fp32;
+ *   bf16 storage with one bf16 product, accumulated in fp32.
+ */
+#ifndef NRC_H_
+#define NRC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NRC_OK = 0,
+    NRC_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, overlap, bad value */
+    NRC_ERR_UNSUPPORTED = 2,   /* well-formed but outside what the kernels implement */
+    NRC_ERR_ALIGNMENT = 3,     /* workspace (or a vector pointer) misaligned */
+    NRC_ERR_WORKSPACE = 4,     /* workspace_bytes smaller than the query returned */
+    NRC_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
+    NRC_ERR_TIMEOUT = 6        /* a device-side wait gave up (nrc_query_status) */
+} nrc_status;
+
+typedef enum {
+    NRC_F32 = 0,               /* x, out, conv weight and conv bias stored fp32 */
+    NRC_BF16 = 1               /* ... stored bf16 (BatchNorm parameters stay fp32) */
+} nrc_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *nrc_status_string(nrc_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int nrc_version(void);
+
+/* ------------------------------------------------------------------------
+ * Pre-norm residual block ("Kimi-K2.6 l2_p12", problem statement)
+ *
+ *   s_c   = gamma[c] / sqrt(running_var[c] + bn_eps)
+ *   z     = max(0, (x - running_mean[c]) * s_c + beta[c])   for 0 <= t < L,
+ *           0 outside (the conv's zero padding applies to z, after BN+ReLU)
+ *   out[n,o,t] = x[n,o,t] + bias[o]
+ *                + sum_c sum_k W[o,c,k] * z[n, c, t - dilation + k*dilation]
+ *
+ * x, out:        (N, C, L), dtype `dt`.  out must not overlap x.
+ * bn_*:          (C) fp32 each (BatchNorm1d eval-mode buffers and affine).
+ * conv_weight:   (C, C, 3), dtype `dt`.
+ * conv_bias:     (C), dtype `dt`, or NULL for no bias.
+ * kernel_size must be 3 and padding must equal dilation (only then does the
+ * output length equal L, which the residual add needs): otherwise
+ * NRC_ERR_UNSUPPORTED.  dilation >= 1.  C <= 2048.
+ * workspace:     >= nrc_prenorm_dilconv_residual_workspace_size(C, dt) bytes;
+ *                it receives the repacked weights on every call.
+ * ------------------------------------------------------------------------ */
+size_t nrc_prenorm_dilconv_residual_workspace_size(int C, nrc_dtype dt);
+
+nrc_status nrc_prenorm_dilconv_residual(
+    const void *x, void *out, nrc_dtype dt, int N, int C, int L,
+    int kernel_size, int dilation, int padding,
+    const float *bn_running_mean, const float *bn_running_var,
+    const float *bn_gamma, const float *bn_beta, float bn_eps,
+    const void *conv_weight, const void *conv_bias,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Conv1d + GroupNorm ("FW-GLM-5-1 l2_p35", problem analysis and its
+ * normalisation kernel)
+ *
+ *   y[n,o,t] = bias[o] + sum_c sum_k W[o,c,k] * x[n, c, t - 1 + k]   (x = 0 outside)
+ *   group g = o / (C_out / num_groups)
+ *   mu, var  = mean and biased variance of y over the group's channels and all t
+ *   out      = (y - mu) / sqrt(var + eps) * gamma[o] + beta[o]
+ *
+ * x: (N, C_in, T) fp32.  out: (N, C_out, T) fp32, must not overlap x; it also
+ * holds y between the two kernels of the call.
+ * conv_weight: (C_out, C_in, 3) fp32.  conv_bias: (C_out) or NULL.
+ * gn_gamma, gn_beta: (C_out) fp32, both NULL for affine=False.
+ * kernel_size 3, stride 1, padding 1, dilation 1 only (else UNSUPPORTED).
+ * C_out % num_groups == 0 (else INVALID_ARG); when C_out > 256 the group
+ * size must divide 256 (else UNSUPPORTED).
+ * ------------------------------------------------------------------------ */
+size_t nrc_conv1d_groupnorm_workspace_size(int N, int C_in, int C_out, int T,
+                                           int num_groups);
+
+nrc_status nrc_conv1d_groupnorm(
+    const float *x, float *out, int N, int C_in, int C_out, int T,
+    int kernel_size, int stride, int padding, int dilation,
+    const float *conv_weight, const float *conv_bias,
+    int num_groups, const float *gn_gamma, const float *gn_beta, float eps,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Linear + BatchNorm1d + scalar bias + divide + Swish ("Kimi-K2.6 l2_p97")
+ *
+ *   y = x W^T + lin_bias                                 (B x out_f)
+ *   training=1: mu_j, var_j = batch mean and biased variance of column j;
+ *               running_mean = (1-m)*running_mean + m*mu
+ *               running_var  = (1-m)*running_var  + m*var*B/(B-1)
+ *               *num_batches_tracked += 1 (if not NULL)
+ *   training=0: mu = running_mean, var = running_var, nothing updated
+ *   u   = ((y - mu)/sqrt(var + eps) * gamma + beta + *add_bias) / divide_value
+ *   out = u * sigmoid(u)
+ *
+ * x: (B, in_f) fp32.  out: (B, out_f) fp32 (holds y between kernels), no
+ * overlap with x.  lin_weight: (out_f, in_f).  lin_bias: (out_f) or NULL.
+ * bn_gamma/bn_beta: (out_f) or both NULL (1 and 0).  running_mean/var:
+ * (out_f), read in eval mode, read and updated in place in training mode.
+ * num_batches_tracked: one int64 or NULL.  add_bias: DEVICE pointer to one
+ * fp32 value (read on the device, so the call never syncs).  divide_value
+ * must be non-zero.  training=1 needs B >= 2 (unbiased variance).
+ * momentum in [0, 1].
+ * ------------------------------------------------------------------------ */
+size_t nrc_linear_bn_swish_workspace_size(int B, int in_f, int out_f);
+
+nrc_status nrc_linear_bn_swish(
+    const float *x, float *out, int B, int in_f, int out_f,
+    const float *lin_weight, const float *lin_bias,
+    const float *bn_gamma, const float *bn_beta,
+    float *bn_running_mean, float *bn_running_var, int64_t *num_batches_tracked,
+    float bn_eps, float bn_momentum, int training,
+    const float *add_bias, float divide_value,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Status and fault handling
+ * ------------------------------------------------------------------------ */
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns NRC_OK, NRC_ERR_TIMEOUT (a device wait gave up; the
+ * kernel returned early and its outputs are undefined) or NRC_ERR_CUDA. */
+nrc_status nrc_query_status(void *stream);
+
+/* Where the last recorded device error happened (a wait-site id, 0 if none). */
+int nrc_last_error_site(void);
+
+/* Limit of every device-side wait, in nanoseconds (default 2e9).  Applies to
+ * launches made after the call. */
+void nrc_set_wait_timeout_ns(uint64_t ns);
+
+/* Fault-path self test: launches one CTA whose thread waits, with the given
+ * limit, on an mbarrier that nothing ever arrives at.  The wait gives up and
+ * records NRC_ERR_TIMEOUT exactly like a stalled pipeline would; the launch
+ * itself returns NRC_OK.  Read the outcome with nrc_query_status. */
+nrc_status nrc_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NRC_H_ */

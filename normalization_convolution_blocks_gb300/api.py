@@ -1,0 +1,270 @@
+"""Thin Python binding over libnrc.so (include/nrc.h), same names as the C ABI.
+
+Argument marshalling only: torch tensors become device pointers, the current
+torch stream becomes the ``stream`` argument, outputs and workspaces are
+allocated with torch.  Every step of every block runs in the library's CUDA
+kernels; there is no CPU fallback -- if the library is not built, or no GPU
+is present, the calls raise.
+
+Host (CPU) input tensors are accepted for end-to-end use: they are copied to
+the current device before the call (non-blocking when pinned) and the result
+is copied back to host memory.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+NRC_OK, NRC_ERR_INVALID_ARG, NRC_ERR_UNSUPPORTED = 0, 1, 2
+NRC_ERR_ALIGNMENT, NRC_ERR_WORKSPACE, NRC_ERR_CUDA, NRC_ERR_TIMEOUT = 3, 4, 5, 6
+NRC_F32, NRC_BF16 = 0, 1
+
+_lib = None
+
+
+class NrcError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libnrc.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libnrc.so not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    p, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    u64 = ctypes.c_uint64
+    sig = {
+        "nrc_status_string": ([i], ctypes.c_char_p),
+        "nrc_version": ([], i),
+        "nrc_prenorm_dilconv_residual_workspace_size": ([i, i], sz),
+        "nrc_prenorm_dilconv_residual": ([p, p, i, i, i, i, i, i, i, p, p, p, p, f, p, p, p, sz,
+                                          p], i),
+        "nrc_conv1d_groupnorm_workspace_size": ([i, i, i, i, i], sz),
+        "nrc_conv1d_groupnorm": ([p, p, i, i, i, i, i, i, i, i, p, p, i, p, p, f, p, sz, p], i),
+        "nrc_linear_bn_swish_workspace_size": ([i, i, i], sz),
+        "nrc_linear_bn_swish": ([p, p, i, i, i, p, p, p, p, p, p, p, f, f, i, p, f, p, sz, p], i),
+        "nrc_query_status": ([p], i),
+        "nrc_last_error_site": ([], i),
+        "nrc_set_wait_timeout_ns": ([u64], None),
+        "nrc_selftest_wait_timeout": ([u64, p], i),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().nrc_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != NRC_OK:
+        raise NrcError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, device, dtype=None):
+    """Device copy of an optional tensor (contiguous, given dtype)."""
+    if t is None:
+        return None
+    t = t.to(device=device, dtype=dtype or t.dtype, non_blocking=True)
+    return t.contiguous()
+
+
+def _workspace(nbytes, device, workspace):
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def _target_device(x):
+    if x.is_cuda:
+        return x.device
+    if not torch.cuda.is_available():
+        raise RuntimeError("nrc needs a CUDA device (no CPU fallback)")
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+# ---------------------------------------------------------------------------
+# Pre-norm residual block
+# ---------------------------------------------------------------------------
+def prenorm_dilconv_residual_workspace_size(C: int, dtype=torch.float32) -> int:
+    dt = NRC_F32 if dtype == torch.float32 else NRC_BF16
+    return int(load().nrc_prenorm_dilconv_residual_workspace_size(C, dt))
+
+
+def prenorm_dilconv_residual(x, bn_running_mean, bn_running_var, bn_gamma, bn_beta, bn_eps,
+                             conv_weight, conv_bias, dilation, padding=None, kernel_size=3,
+                             out=None, workspace=None, stream=None):
+    """out = x + Conv1d(ReLU(BatchNorm1d_eval(x))) with k=3, padding=dilation.
+
+    x (N, C, L) fp32 or bf16; BN tensors (C) fp32; conv_weight (C, C, 3) and
+    conv_bias (C) in x's dtype (bias may be None)."""
+    lib = load()
+    host = not x.is_cuda
+    dev = _target_device(x)
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be float32 or bfloat16")
+    dt = NRC_F32 if x.dtype == torch.float32 else NRC_BF16
+    xd = _dev(x, dev)
+    N, C, L = xd.shape
+    rm, rv, g, b = (_dev(t, dev, torch.float32) for t in (bn_running_mean, bn_running_var,
+                                                           bn_gamma, bn_beta))
+    w = _dev(conv_weight, dev, x.dtype)
+    cb = _dev(conv_bias, dev, x.dtype)
+    padding = dilation if padding is None else padding
+    o = out if (out is not None and not host) else torch.empty_like(xd)
+    need = lib.nrc_prenorm_dilconv_residual_workspace_size(C, dt)
+    ws = _workspace(need, dev, workspace)
+    st = lib.nrc_prenorm_dilconv_residual(
+        _ptr(xd), _ptr(o), dt, N, C, L, kernel_size, dilation, padding, _ptr(rm), _ptr(rv),
+        _ptr(g), _ptr(b), float(bn_eps), _ptr(w), _ptr(cb), _ptr(ws), ws.numel(),
+        _stream(stream))
+    _check(st, "nrc_prenorm_dilconv_residual")
+    _keep_alive(stream, xd, rm, rv, g, b, w, cb, ws)
+    if host:
+        res = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        res.copy_(o, non_blocking=False)
+        return res
+    return o
+
+
+def _keep_alive(stream, *tensors):
+    """Temporaries used on a non-current stream must not be recycled early."""
+    if stream is None:
+        return
+    for t in tensors:
+        if t is not None and t.is_cuda:
+            t.record_stream(stream)
+
+
+# ---------------------------------------------------------------------------
+# Conv1d + GroupNorm
+# ---------------------------------------------------------------------------
+def conv1d_groupnorm_workspace_size(N, C_in, C_out, T, num_groups) -> int:
+    return int(load().nrc_conv1d_groupnorm_workspace_size(N, C_in, C_out, T, num_groups))
+
+
+def conv1d_groupnorm(x, conv_weight, conv_bias, num_groups, gn_gamma, gn_beta, eps=1e-5,
+                     kernel_size=3, stride=1, padding=1, dilation=1, out=None, workspace=None,
+                     stream=None):
+    """GroupNorm(num_groups)(Conv1d(x)); x (N, C_in, T) fp32, conv_weight (C_out, C_in, 3)."""
+    lib = load()
+    host = not x.is_cuda
+    dev = _target_device(x)
+    xd = _dev(x, dev, torch.float32)
+    N, Cin, T = xd.shape
+    w = _dev(conv_weight, dev, torch.float32)
+    Cout = w.shape[0]
+    cb, g, b = (_dev(t, dev, torch.float32) for t in (conv_bias, gn_gamma, gn_beta))
+    o = out if (out is not None and not host) else torch.empty((N, Cout, T), device=dev,
+                                                                dtype=torch.float32)
+    ws = _workspace(lib.nrc_conv1d_groupnorm_workspace_size(N, Cin, Cout, T, num_groups), dev,
+                    workspace)
+    st = lib.nrc_conv1d_groupnorm(_ptr(xd), _ptr(o), N, Cin, Cout, T, kernel_size, stride,
+                                  padding, dilation, _ptr(w), _ptr(cb), num_groups, _ptr(g),
+                                  _ptr(b), float(eps), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "nrc_conv1d_groupnorm")
+    _keep_alive(stream, xd, w, cb, g, b, ws)
+    if host:
+        res = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        res.copy_(o)
+        return res
+    return o
+
+
+# ---------------------------------------------------------------------------
+# Linear + BatchNorm1d + bias + divide + Swish
+# ---------------------------------------------------------------------------
+def linear_bn_swish_workspace_size(B, in_f, out_f) -> int:
+    return int(load().nrc_linear_bn_swish_workspace_size(B, in_f, out_f))
+
+
+def linear_bn_swish(x, lin_weight, lin_bias, bn_gamma, bn_beta, bn_running_mean,
+                    bn_running_var, add_bias, divide_value=1.0, bn_eps=1e-5, bn_momentum=0.1,
+                    training=True, num_batches_tracked=None, out=None, workspace=None,
+                    stream=None):
+    """Swish((BatchNorm1d(Linear(x)) + add_bias) / divide_value).
+
+    In training mode bn_running_mean/var (device fp32 tensors) and
+    num_batches_tracked (device int64 tensor or None) are updated in place.
+    add_bias is a one-element tensor (read on the device)."""
+    lib = load()
+    host = not x.is_cuda
+    dev = _target_device(x)
+    xd = _dev(x, dev, torch.float32)
+    B, IN = xd.shape
+    w = _dev(lin_weight, dev, torch.float32)
+    OUT = w.shape[0]
+    lb, g, b = (_dev(t, dev, torch.float32) for t in (lin_bias, bn_gamma, bn_beta))
+    for t in (bn_running_mean, bn_running_var):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise TypeError("running statistics must be contiguous fp32 device tensors")
+    if num_batches_tracked is not None and not (num_batches_tracked.is_cuda and
+                                                num_batches_tracked.dtype == torch.int64):
+        raise TypeError("num_batches_tracked must be an int64 device tensor")
+    ab = _dev(torch.as_tensor(add_bias, dtype=torch.float32).reshape(1), dev, torch.float32)
+    o = out if (out is not None and not host) else torch.empty((B, OUT), device=dev,
+                                                                dtype=torch.float32)
+    ws = _workspace(lib.nrc_linear_bn_swish_workspace_size(B, IN, OUT), dev, workspace)
+    st = lib.nrc_linear_bn_swish(_ptr(xd), _ptr(o), B, IN, OUT, _ptr(w), _ptr(lb), _ptr(g),
+                                 _ptr(b), _ptr(bn_running_mean), _ptr(bn_running_var),
+                                 _ptr(num_batches_tracked), float(bn_eps), float(bn_momentum),
+                                 int(bool(training)), _ptr(ab), float(divide_value), _ptr(ws),
+                                 ws.numel(), _stream(stream))
+    _check(st, "nrc_linear_bn_swish")
+    _keep_alive(stream, xd, w, lb, g, b, ab, ws)
+    if host:
+        res = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        res.copy_(o)
+        return res
+    return o
+
+
+# ---------------------------------------------------------------------------
+# Status
+# ---------------------------------------------------------------------------
+def query_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return int(load().nrc_query_status(_stream(stream)))
+
+
+def last_error_site() -> int:
+    return int(load().nrc_last_error_site())
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    load().nrc_set_wait_timeout_ns(int(ns))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(load().nrc_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+           "nrc_selftest_wait_timeout")

@@ -1,0 +1,117 @@
+// Library-wide pieces of libnrc.so: the device status word, status queries,
+// the wait-limit setting and the fault-path self test.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "nrc_host.h"
+#include "nrc_ptx.cuh"
+
+namespace nrc {
+
+// Device status word: [0] = first error code recorded, [1] = where (wait site).
+__device__ int g_status_word[2];
+
+namespace {
+constexpr int kMaxDevices = 64;
+int* g_status_addr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+std::mutex g_mu;
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+int g_last_site = 0;
+
+int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+    return d;
+}
+}  // namespace
+
+int* device_status_ptr() {
+    const int d = current_device();
+    if (d < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_addr[d]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_addr[d] = static_cast<int*>(p);
+    }
+    return g_status_addr[d];
+}
+
+unsigned long long wait_timeout_ns() { return g_timeout_ns.load(); }
+
+int device_sm_count() {
+    const int d = current_device();
+    if (d < 0) return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sm_count[d]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+        g_sm_count[d] = n > 0 ? n : 1;
+    }
+    return g_sm_count[d];
+}
+
+// One thread waits, with a bounded limit, on an mbarrier that nothing arrives
+// at; the give-up path records the timeout like a stalled pipeline would.
+__global__ void selftest_wait_timeout_kernel(int* status, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+        WaitCtx ctx{&abort_flag, status, limit_ns};
+        mbar_wait(smem_u32(&bar), 0, ctx, 99);
+    }
+}
+
+}  // namespace nrc
+
+using namespace nrc;
+
+extern "C" const char* nrc_status_string(nrc_status s) {
+    switch (s) {
+        case NRC_OK: return "NRC_OK";
+        case NRC_ERR_INVALID_ARG: return "NRC_ERR_INVALID_ARG";
+        case NRC_ERR_UNSUPPORTED: return "NRC_ERR_UNSUPPORTED";
+        case NRC_ERR_ALIGNMENT: return "NRC_ERR_ALIGNMENT";
+        case NRC_ERR_WORKSPACE: return "NRC_ERR_WORKSPACE";
+        case NRC_ERR_CUDA: return "NRC_ERR_CUDA";
+        case NRC_ERR_TIMEOUT: return "NRC_ERR_TIMEOUT";
+    }
+    return "NRC_ERR_UNKNOWN";
+}
+
+extern "C" int nrc_version(void) { return 100; }
+
+extern "C" void nrc_set_wait_timeout_ns(uint64_t ns) {
+    g_timeout_ns.store(ns > 0 ? (unsigned long long)ns : 1ull);
+}
+
+extern "C" int nrc_last_error_site(void) { return g_last_site; }
+
+extern "C" nrc_status nrc_query_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return NRC_ERR_CUDA;
+    int word[2] = {0, 0};
+    if (cudaMemcpyFromSymbol(word, g_status_word, sizeof(word)) != cudaSuccess)
+        return NRC_ERR_CUDA;
+    if (word[0] != 0) {
+        g_last_site = word[1];
+        const int zero[2] = {0, 0};
+        if (cudaMemcpyToSymbol(g_status_word, zero, sizeof(zero)) != cudaSuccess)
+            return NRC_ERR_CUDA;
+    }
+    return word[0] == 0 ? NRC_OK : static_cast<nrc_status>(word[0]);
+}
+
+extern "C" nrc_status nrc_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+    int* status = device_status_ptr();
+    if (!status) return NRC_ERR_CUDA;
+    selftest_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        status, (unsigned long long)limit_ns);
+    return cuda_status(cudaGetLastError());
+}

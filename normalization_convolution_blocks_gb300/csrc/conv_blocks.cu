@@ -1,0 +1,478 @@
+// Conv1d blocks as implicit GEMMs on tcgen05:
+//   * pre-norm residual block  out = x + Conv1d(ReLU(BN_eval(x))), k=3, pad=dil
+//     ("Kimi-K2.6 l2_p12", problem statement)
+//   * Conv1d(k=3, pad=1) + GroupNorm ("FW-GLM-5-1 l2_p35", problem analysis)
+//
+// GEMM view of one sample n: D[t][o] = sum_tap sum_c z[c][t - pad + tap*dil] * W[o][c][tap].
+// Tile rows are 128 consecutive t, tile columns BN output channels; the K loop
+// runs over (tap, 64-channel chunk).  The A operand (activations) is produced
+// in shared memory by the prologue warps: the conv input for the tile's shifted
+// window, with BN+ReLU applied (block) and the zero padding applied after it,
+// split into bf16 hi/lo parts for fp32 storage.  The B operand (weights) is
+// repacked once per call into the exact shared-memory image the MMA reads.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "nrc_launch.cuh"
+
+namespace nrc {
+
+template <typename T>
+__device__ __forceinline__ float load_f(const T* p);
+template <>
+__device__ __forceinline__ float load_f<float>(const float* p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const unsigned short u = __ldg(reinterpret_cast<const unsigned short*>(p));
+    return __uint_as_float((uint32_t)u << 16);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_f(T* p, float v);
+template <>
+__device__ __forceinline__ void store_f<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void store_f<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+    *p = __float2bfloat16_rn(v);
+}
+
+enum class ConvEpi { kResidual, kGroupStats };
+
+struct ConvParams {
+    const void* x;          // (N, Cin, L)
+    void* out;              // (N, Cout, L)
+    int N, Cin, Cout, L;
+    int pad, dil;           // tap k of output t reads t - pad + k*dil
+    int n_tt, n_ot, n_chunks, n_kiters, BN;
+    // eval-mode BatchNorm of the block's prologue (NULL rm: no BN/ReLU)
+    const float *rm, *rv, *gamma, *beta;
+    float bn_eps;
+    const void* bias;       // (Cout) or NULL
+    const uint8_t* wpack;   // packed weight image
+    // group statistics (conv + GroupNorm)
+    float4* partials;       // [(n*G + g) * n_tt * 4 + tt*4 + quarter] = (count, mean, M2, 0)
+    int G, cpg;
+};
+
+// Tile index -> (n, t tile, o tile); o tiles of one (n, t) are adjacent, then t,
+// so neighbouring CTAs share the x windows (and the +-dil halos) in L2.
+struct ConvTile {
+    int n, tt, ot;
+};
+__device__ __forceinline__ ConvTile conv_tile(const ConvParams& p, int tile) {
+    ConvTile r;
+    r.ot = tile % p.n_ot;
+    const int rest = tile / p.n_ot;
+    r.tt = rest % p.n_tt;
+    r.n = rest / p.n_tt;
+    return r;
+}
+
+// Warp-level merge of (count, mean, M2) triples (Chan et al.'s pairwise
+// update); every lane ends with the total.  Lanes with count 0 contribute
+// nothing.
+__device__ __forceinline__ void warp_merge_stats(float& cnt, float& mean, float& m2) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float nb = __shfl_xor_sync(0xffffffffu, cnt, off);
+        const float mb = __shfl_xor_sync(0xffffffffu, mean, off);
+        const float qb = __shfl_xor_sync(0xffffffffu, m2, off);
+        const float nab = cnt + nb;
+        if (nab > 0.f) {
+            const float delta = mb - mean;
+            const float fb = nb / nab;
+            mean = mean + delta * fb;
+            m2 = m2 + qb + delta * delta * cnt * fb;
+            cnt = nab;
+        }
+    }
+}
+
+template <typename T, ConvEpi EPI>
+struct ConvProblem {
+    using Params = ConvParams;
+
+    static __device__ void setup(const Params& p, uint8_t* extra) {
+        if (p.rm == nullptr) return;
+        // BN fold: z = max(0, x*scale + shift), scale = gamma/sqrt(rv+eps),
+        // shift = beta - rm*scale.  Channels past Cin get 0 (never used: guarded).
+        float* sc = reinterpret_cast<float*>(extra);
+        float* sh = sc + p.n_chunks * kBK;
+        for (int c = threadIdx.x; c < p.n_chunks * kBK; c += blockDim.x) {
+            float s = 0.f, h = 0.f;
+            if (c < p.Cin) {
+                s = p.gamma[c] / sqrtf(p.rv[c] + p.bn_eps);
+                h = p.beta[c] - p.rm[c] * s;
+            }
+            sc[c] = s;
+            sh[c] = h;
+        }
+    }
+
+    static __device__ __forceinline__ void fetch_a(const Params& p, const uint8_t* extra,
+                                                   int tile, int kiter, int row, int k0,
+                                                   float (&v)[32]) {
+        const ConvTile tl = conv_tile(p, tile);
+        const int tap = kiter / p.n_chunks;
+        const int chunk = kiter - tap * p.n_chunks;
+        const int t = tl.tt * kBM + row;
+        const int s = t - p.pad + tap * p.dil;
+        const bool s_ok = (unsigned)s < (unsigned)p.L;
+        const int c0 = chunk * kBK + k0;
+        const T* xp = static_cast<const T*>(p.x) + ((size_t)tl.n * p.Cin + c0) * p.L + s;
+        float raw[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            raw[i] = (s_ok && c0 + i < p.Cin) ? load_f<T>(xp + (size_t)i * p.L) : 0.f;
+        if (p.rm != nullptr) {
+            const float* sc = reinterpret_cast<const float*>(extra) + c0;
+            const float* sh = reinterpret_cast<const float*>(extra) + p.n_chunks * kBK + c0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)   // zero padding applies to z, after BN+ReLU
+                v[i] = s_ok ? fmaxf(fmaf(raw[i], sc[i], sh[i]), 0.f) : 0.f;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = raw[i];
+        }
+    }
+
+    static __device__ __forceinline__ const void* b_src(const Params& p, int tile, int kiter) {
+        const int ot = tile % p.n_ot;
+        constexpr int NP = sizeof(T) == 4 ? 2 : 1;
+        return p.wpack + ((size_t)ot * p.n_kiters + kiter) * NP * (size_t)p.BN * 128u;
+    }
+
+    static __device__ __forceinline__ void epilogue(const Params& p, const uint8_t*, int tile,
+                                                    int quarter, int lane, uint32_t taddr,
+                                                    int BN) {
+        const ConvTile tl = conv_tile(p, tile);
+        const int t = tl.tt * kBM + quarter * 32 + lane;
+        const bool t_ok = t < p.L;
+        const T* bias = static_cast<const T*>(p.bias);
+        T* out = static_cast<T*>(p.out);
+        const int obase = tl.ot * BN;
+        const size_t row0 = (size_t)tl.n * p.Cout;
+        if constexpr (EPI == ConvEpi::kResidual) {
+            const T* x = static_cast<const T*>(p.x);
+            for (int cc = 0; cc < BN; cc += 16) {
+                float r[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int o = obase + cc + i;
+                    r[i] = (t_ok && o < p.Cout) ? load_f<T>(x + (row0 + o) * p.L + t) : 0.f;
+                }
+                float v[16];
+                tmem_ld16(taddr + (uint32_t)cc, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int o = obase + cc + i;
+                    if (t_ok && o < p.Cout) {
+                        const float b = bias ? load_f<T>(bias + o) : 0.f;
+                        store_f<T>(out + (row0 + o) * p.L + t, v[i] + b + r[i]);
+                    }
+                }
+            }
+        } else {
+            // y -> out, and per-(n, group, t tile, warp) statistics of y.
+            float cnt = 0.f, mean = 0.f, m2 = 0.f;
+            for (int cc = 0; cc < BN; cc += 16) {
+                float v[16];
+                tmem_ld16(taddr + (uint32_t)cc, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int col = cc + i;
+                    const int o = obase + col;
+                    if (o >= p.Cout) break;                 // uniform across the warp
+                    const float y = v[i] + (bias ? load_f<T>(bias + o) : 0.f);
+                    if (t_ok) {
+                        store_f<T>(out + (row0 + o) * p.L + t, y);
+                        cnt += 1.f;                          // Welford update
+                        const float d = y - mean;
+                        mean += d / cnt;
+                        m2 += d * (y - mean);
+                    }
+                    if ((o + 1) % p.cpg == 0) {              // last channel of group
+                        warp_merge_stats(cnt, mean, m2);
+                        if (lane == 0) {
+                            const int g = o / p.cpg;
+                            p.partials[((size_t)(tl.n * p.G + g) * p.n_tt + tl.tt) * 4 + quarter] =
+                                make_float4(cnt, mean, m2, 0.f);
+                        }
+                        cnt = 0.f;
+                        mean = 0.f;
+                        m2 = 0.f;
+                    }
+                }
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Weight repack: W (Cout, Cin, 3) -> for each (o tile, tap, 64-channel chunk)
+// the B-stage image: NP parts of BN rows x 64 bf16, 128B-swizzled.  fp32
+// weights are split into hi + lo bf16 parts; bf16 weights are copied.  Rows
+// past Cout and channels past Cin are zero.  One thread per 16-byte chunk.
+// ---------------------------------------------------------------------------
+template <typename T, int NP>
+__global__ void pack_conv_weight_kernel(const T* __restrict__ w, uint8_t* __restrict__ pack,
+                                        int Cout, int Cin, int BN, int n_ot, int n_chunks) {
+    const int n_kiters = 3 * n_chunks;
+    const size_t total = (size_t)n_ot * n_kiters * BN * 8;   // 16-byte chunks per part
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int j = (int)(idx & 7);
+        size_t rest = idx >> 3;
+        const int row = (int)(rest % BN);
+        rest /= BN;
+        const int kiter = (int)(rest % n_kiters);
+        const int ot = (int)(rest / n_kiters);
+        const int tap = kiter / n_chunks, chunk = kiter % n_chunks;
+        const int o = ot * BN + row;
+        const int c0 = chunk * kBK + j * 8;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = c0 + e;
+            v[e] = (o < Cout && c < Cin) ? load_f<T>(w + ((size_t)o * Cin + c) * 3 + tap) : 0.f;
+        }
+        const size_t blk = ((size_t)ot * n_kiters + kiter) * NP;
+        const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)j);
+        uint4* hi = reinterpret_cast<uint4*>(pack + (blk * BN) * 128 + off);
+        if constexpr (NP == 2) {
+            uint32_t h[4], l[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_bf16x2(v[2 * e], v[2 * e + 1], h[e], l[e]);
+            *hi = make_uint4(h[0], h[1], h[2], h[3]);
+            uint4* lo = reinterpret_cast<uint4*>(pack + ((blk + 1) * BN) * 128 + off);
+            *lo = make_uint4(l[0], l[1], l[2], l[3]);
+        } else {
+            // bf16 input: values are already bf16, the repack is exact.
+            *hi = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                             pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// GroupNorm finalize + normalize, one CTA per (n, group): merge the partial
+// (count, mean, M2) of the group in a fixed order, then
+// out = (y - mean) * rsqrt(var + eps) * gamma + beta in place over the group's
+// contiguous (cpg x T) block.
+// ---------------------------------------------------------------------------
+__global__ void groupnorm_finalize_normalize_kernel(float* __restrict__ out,
+                                                    const float4* __restrict__ partials,
+                                                    int n_part, int Cout, int T, int G,
+                                                    const float* __restrict__ gamma,
+                                                    const float* __restrict__ beta, float eps) {
+    const int ng = blockIdx.x;
+    const int g = ng % G;
+    const int cpg = Cout / G;
+    __shared__ float s_mean, s_inv;
+    if (threadIdx.x < 32) {
+        float cnt = 0.f, mean = 0.f, m2 = 0.f;
+        for (int i = threadIdx.x; i < n_part; i += 32) {
+            const float4 q = partials[(size_t)ng * n_part + i];
+            const float nab = cnt + q.x;
+            if (nab > 0.f) {
+                const float delta = q.y - mean;
+                const float fb = q.x / nab;
+                mean += delta * fb;
+                m2 += q.z + delta * delta * cnt * fb;
+                cnt = nab;
+            }
+        }
+        warp_merge_stats(cnt, mean, m2);
+        if (threadIdx.x == 0) {
+            const float var = fmaxf(m2 / cnt, 0.f);   // biased variance
+            s_mean = mean;
+            s_inv = 1.0f / sqrtf(var + eps);
+        }
+    }
+    __syncthreads();
+    const float mean = s_mean, inv = s_inv;
+    float* base = out + (size_t)ng * cpg * T;      // channels g*cpg.. of sample n
+    const size_t cnt = (size_t)cpg * T;
+    if ((T & 3) == 0) {
+        float4* b4 = reinterpret_cast<float4*>(base);
+        for (size_t i = threadIdx.x; i < cnt / 4; i += blockDim.x) {
+            const int o = g * cpg + (int)((i * 4) / T);
+            const float a = inv * (gamma ? gamma[o] : 1.f);
+            const float c = (beta ? beta[o] : 0.f) - mean * a;
+            float4 y = b4[i];
+            y.x = fmaf(y.x, a, c);
+            y.y = fmaf(y.y, a, c);
+            y.z = fmaf(y.z, a, c);
+            y.w = fmaf(y.w, a, c);
+            b4[i] = y;
+        }
+    } else {
+        for (size_t i = threadIdx.x; i < cnt; i += blockDim.x) {
+            const int o = g * cpg + (int)(i / T);
+            const float a = inv * (gamma ? gamma[o] : 1.f);
+            const float c = (beta ? beta[o] : 0.f) - mean * a;
+            base[i] = fmaf(base[i], a, c);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+struct ConvPlan {
+    GemmPlan g;
+    int n_ot, n_chunks, n_tt;
+    size_t wpack_bytes;
+};
+
+static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn) {
+    ConvPlan pl{};
+    const int BN = Cout <= 256 ? ((Cout + 15) / 16) * 16 : 256;
+    pl.n_ot = ceil_div(Cout, BN);
+    pl.n_chunks = ceil_div(Cin, kBK);
+    pl.n_tt = ceil_div(L, kBM);
+    const long long tiles = (long long)N * pl.n_tt * pl.n_ot;
+    const uint32_t extra = with_bn ? (uint32_t)(2 * pl.n_chunks * kBK * 4) : 0u;
+    pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), 3 * pl.n_chunks, NP,
+                          extra);
+    pl.wpack_bytes = (size_t)pl.n_ot * pl.g.num_kiters * NP * BN * 128;
+    return pl;
+}
+
+}  // namespace nrc
+
+using namespace nrc;
+
+extern "C" size_t nrc_prenorm_dilconv_residual_workspace_size(int C, nrc_dtype dt) {
+    if (C <= 0 || (dt != NRC_F32 && dt != NRC_BF16)) return 0;
+    return plan_conv(1, C, C, 1, dt == NRC_F32 ? 2 : 1, true).wpack_bytes;
+}
+
+extern "C" nrc_status nrc_prenorm_dilconv_residual(
+    const void* x, void* out, nrc_dtype dt, int N, int C, int L, int kernel_size, int dilation,
+    int padding, const float* rm, const float* rv, const float* gamma, const float* beta,
+    float bn_eps, const void* conv_weight, const void* conv_bias, void* workspace,
+    size_t workspace_bytes, void* stream) {
+    if (dt != NRC_F32 && dt != NRC_BF16) return NRC_ERR_INVALID_ARG;
+    if (!x || !out || !rm || !rv || !gamma || !beta || !conv_weight || !workspace)
+        return NRC_ERR_INVALID_ARG;
+    if (N <= 0 || C <= 0 || L <= 0 || dilation <= 0 || padding < 0) return NRC_ERR_INVALID_ARG;
+    if (!(bn_eps >= 0.f) || !std::isfinite(bn_eps)) return NRC_ERR_INVALID_ARG;
+    if (kernel_size != 3 || padding != dilation) return NRC_ERR_UNSUPPORTED;
+    if (C > 2048) return NRC_ERR_UNSUPPORTED;
+    const size_t esz = dt == NRC_F32 ? 4 : 2;
+    const size_t bytes = (size_t)N * C * L * esz;
+    if (ranges_overlap(x, bytes, out, bytes)) return NRC_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return NRC_ERR_ALIGNMENT;
+    const int NP = dt == NRC_F32 ? 2 : 1;
+    const ConvPlan pl = plan_conv(N, C, C, L, NP, true);
+    if (workspace_bytes < pl.wpack_bytes) return NRC_ERR_WORKSPACE;
+    if ((long long)N * pl.n_tt * pl.n_ot >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ConvParams p{};
+    p.x = x;
+    p.out = out;
+    p.N = N;
+    p.Cin = C;
+    p.Cout = C;
+    p.L = L;
+    p.pad = padding;
+    p.dil = dilation;
+    p.n_tt = pl.n_tt;
+    p.n_ot = pl.n_ot;
+    p.n_chunks = pl.n_chunks;
+    p.n_kiters = pl.g.num_kiters;
+    p.BN = pl.g.BN;
+    p.rm = rm;
+    p.rv = rv;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.bn_eps = bn_eps;
+    p.bias = conv_bias;
+    p.wpack = static_cast<const uint8_t*>(workspace);
+    const size_t units = pl.wpack_bytes / 16 / NP;
+    if (dt == NRC_F32) {
+        pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
+            static_cast<const float*>(conv_weight), static_cast<uint8_t*>(workspace), C, C,
+            pl.g.BN, pl.n_ot, pl.n_chunks);
+        if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
+        return launch_gemm<ConvProblem<float, ConvEpi::kResidual>, 2>(p, pl.g, st);
+    }
+    pack_conv_weight_kernel<__nv_bfloat16, 1><<<elementwise_grid(units), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(conv_weight), static_cast<uint8_t*>(workspace), C, C,
+        pl.g.BN, pl.n_ot, pl.n_chunks);
+    if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
+    return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual>, 1>(p, pl.g, st);
+}
+
+static size_t gn_partials_offset(const ConvPlan& pl) {
+    return (pl.wpack_bytes + 255) & ~(size_t)255;
+}
+
+extern "C" size_t nrc_conv1d_groupnorm_workspace_size(int N, int C_in, int C_out, int T,
+                                                      int num_groups) {
+    if (N <= 0 || C_in <= 0 || C_out <= 0 || T <= 0 || num_groups <= 0) return 0;
+    const ConvPlan pl = plan_conv(N, C_in, C_out, T, 2, false);
+    return gn_partials_offset(pl) + (size_t)N * num_groups * pl.n_tt * 4 * sizeof(float4);
+}
+
+extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, int C_in, int C_out,
+                                           int T, int kernel_size, int stride, int padding,
+                                           int dilation, const float* conv_weight,
+                                           const float* conv_bias, int num_groups,
+                                           const float* gn_gamma, const float* gn_beta, float eps,
+                                           void* workspace, size_t workspace_bytes,
+                                           void* stream) {
+    if (!x || !out || !conv_weight || !workspace) return NRC_ERR_INVALID_ARG;
+    if (N <= 0 || C_in <= 0 || C_out <= 0 || T <= 0 || num_groups <= 0)
+        return NRC_ERR_INVALID_ARG;
+    if ((gn_gamma == nullptr) != (gn_beta == nullptr)) return NRC_ERR_INVALID_ARG;
+    if (C_out % num_groups != 0) return NRC_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return NRC_ERR_INVALID_ARG;
+    if (kernel_size != 3 || stride != 1 || padding != 1 || dilation != 1)
+        return NRC_ERR_UNSUPPORTED;
+    const int cpg = C_out / num_groups;
+    if (C_out > 256 && 256 % cpg != 0) return NRC_ERR_UNSUPPORTED;
+    if (ranges_overlap(x, (size_t)N * C_in * T * 4, out, (size_t)N * C_out * T * 4))
+        return NRC_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return NRC_ERR_ALIGNMENT;
+    const ConvPlan pl = plan_conv(N, C_in, C_out, T, 2, false);
+    if (workspace_bytes < nrc_conv1d_groupnorm_workspace_size(N, C_in, C_out, T, num_groups))
+        return NRC_ERR_WORKSPACE;
+    if ((long long)N * pl.n_tt * pl.n_ot >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    ConvParams p{};
+    p.x = x;
+    p.out = out;
+    p.N = N;
+    p.Cin = C_in;
+    p.Cout = C_out;
+    p.L = T;
+    p.pad = 1;
+    p.dil = 1;
+    p.n_tt = pl.n_tt;
+    p.n_ot = pl.n_ot;
+    p.n_chunks = pl.n_chunks;
+    p.n_kiters = pl.g.num_kiters;
+    p.BN = pl.g.BN;
+    p.bias = conv_bias;
+    p.wpack = ws;
+    p.partials = reinterpret_cast<float4*>(ws + gn_partials_offset(pl));
+    p.G = num_groups;
+    p.cpg = cpg;
+    const size_t units = pl.wpack_bytes / 16 / 2;
+    pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
+        conv_weight, ws, C_out, C_in, pl.g.BN, pl.n_ot, pl.n_chunks);
+    if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
+    nrc_status s = launch_gemm<ConvProblem<float, ConvEpi::kGroupStats>, 2>(p, pl.g, st);
+    if (s != NRC_OK) return s;
+    groupnorm_finalize_normalize_kernel<<<N * num_groups, 256, 0, st>>>(
+        out, p.partials, pl.n_tt * 4, C_out, T, num_groups, gn_gamma, gn_beta, eps);
+    return cuda_status(cudaGetLastError());
+}

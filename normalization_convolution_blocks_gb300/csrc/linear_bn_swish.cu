@@ -1,0 +1,298 @@
+// Linear + BatchNorm1d + scalar bias + divide + Swish ("Kimi-K2.6 l2_p97").
+//
+// GEMM orientation: tile rows are 128 output features j (A = rows of the Linear
+// weight, converted to bf16 hi/lo by the prologue warps straight from fp32, so
+// the large weight is never rewritten), tile columns are BN batch rows b (B =
+// x, split into bf16 hi/lo once per call into the shared-memory image).
+// D[j][b] = y[b][j] - lin_bias[j].  With features on TMEM lanes, each thread
+// owns one column j of y: its epilogue stores y (coalesced across the warp)
+// and keeps the column's (count, mean, M2) over the tile's batch rows, so the
+// batch statistics need no cross-thread reduction.
+//
+// Launches per call: pack x -> GEMM (y + per-tile column statistics) ->
+// finalize (batch mean/var, running-stat update) -> normalize + bias +
+// divide + Swish in place.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "nrc_launch.cuh"
+
+namespace nrc {
+
+struct LinearParams {
+    const float* W;          // (OUT, IN)
+    const uint8_t* xpack;    // packed x image
+    float* out;              // (B, OUT): receives y
+    const float* lin_bias;   // (OUT) or NULL
+    float4* partials;        // [bt * OUT + j] = (count, mean, M2, 0)
+    int B, IN, OUT;
+    int n_jt, n_bt, n_kiters, BN;
+    int vec_ok;              // W 16-byte aligned and IN % 4 == 0
+};
+
+struct LinearProblem {
+    using Params = LinearParams;
+
+    static __device__ void setup(const Params&, uint8_t*) {}
+
+    static __device__ __forceinline__ void fetch_a(const Params& p, const uint8_t*, int tile,
+                                                   int kiter, int row, int k0,
+                                                   float (&v)[32]) {
+        const int jt = tile / p.n_bt;
+        const int j = jt * kBM + row;
+        const int k = kiter * kBK + k0;
+        if (j >= p.OUT) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            return;
+        }
+        const float* wr = p.W + (size_t)j * p.IN + k;
+        if (p.vec_ok && k + 32 <= p.IN) {
+            const float4* w4 = reinterpret_cast<const float4*>(wr);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q = __ldg(w4 + i);
+                v[4 * i] = q.x;
+                v[4 * i + 1] = q.y;
+                v[4 * i + 2] = q.z;
+                v[4 * i + 3] = q.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = (k + i < p.IN) ? __ldg(wr + i) : 0.f;
+        }
+    }
+
+    static __device__ __forceinline__ const void* b_src(const Params& p, int tile, int kiter) {
+        const int bt = tile % p.n_bt;
+        return p.xpack + ((size_t)bt * p.n_kiters + kiter) * 2 * (size_t)p.BN * 128u;
+    }
+
+    static __device__ __forceinline__ void epilogue(const Params& p, const uint8_t*, int tile,
+                                                    int quarter, int lane, uint32_t taddr,
+                                                    int BN) {
+        const int jt = tile / p.n_bt, bt = tile % p.n_bt;
+        const int j = jt * kBM + quarter * 32 + lane;
+        const bool j_ok = j < p.OUT;
+        const float lb = (j_ok && p.lin_bias) ? __ldg(p.lin_bias + j) : 0.f;
+        const int b0 = bt * BN;
+        float cnt = 0.f, mean = 0.f, m2 = 0.f;
+        for (int cc = 0; cc < BN; cc += 16) {
+            float v[16];
+            tmem_ld16(taddr + (uint32_t)cc, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int b = b0 + cc + i;
+                if (j_ok && b < p.B) {
+                    const float y = v[i] + lb;
+                    p.out[(size_t)b * p.OUT + j] = y;
+                    cnt += 1.f;                       // Welford over the tile's rows
+                    const float d = y - mean;
+                    mean += d / cnt;
+                    m2 += d * (y - mean);
+                }
+            }
+        }
+        if (j_ok) p.partials[(size_t)bt * p.OUT + j] = make_float4(cnt, mean, m2, 0.f);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// x (B, IN) fp32 -> per (batch tile, 64-wide K chunk) the B-stage image: hi and
+// lo bf16 parts of BN rows x 64, 128B-swizzled; rows past B, columns past IN 0.
+// ---------------------------------------------------------------------------
+__global__ void pack_rows_split_kernel(const float* __restrict__ x, uint8_t* __restrict__ pack,
+                                       int B, int IN, int BN, int n_bt, int n_kiters) {
+    const size_t total = (size_t)n_bt * n_kiters * BN * 8;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int j = (int)(idx & 7);
+        size_t rest = idx >> 3;
+        const int row = (int)(rest % BN);
+        rest /= BN;
+        const int kiter = (int)(rest % n_kiters);
+        const int bt = (int)(rest / n_kiters);
+        const int b = bt * BN + row;
+        const int k0 = kiter * kBK + j * 8;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            v[e] = (b < B && k0 + e < IN) ? __ldg(x + (size_t)b * IN + k0 + e) : 0.f;
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_bf16x2(v[2 * e], v[2 * e + 1], h[e], l[e]);
+        const size_t blk = ((size_t)bt * n_kiters + kiter) * 2;
+        const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)j);
+        *reinterpret_cast<uint4*>(pack + blk * BN * 128 + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(pack + (blk + 1) * BN * 128 + off) =
+            make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Per column j: merge the per-batch-tile (count, mean, M2) in a fixed order
+// into the batch mean and biased variance; in training mode update the
+// running statistics (unbiased variance) and num_batches_tracked; emit the
+// column's (centre, scale, shift) so that
+//   u = (y - centre) * scale + shift = ((y - mu)/sqrt(var + eps)*gamma + beta + bias)/div.
+// ---------------------------------------------------------------------------
+__global__ void bn_finalize_kernel(const float4* __restrict__ partials, int n_bt, int B, int OUT,
+                                   const float* __restrict__ gamma, const float* __restrict__ beta,
+                                   float* __restrict__ running_mean, float* __restrict__ running_var,
+                                   long long* __restrict__ nbt, float eps, float momentum,
+                                   int training, const float* __restrict__ add_bias,
+                                   float divide_value, float* __restrict__ colp) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (training && nbt && j == 0) *nbt += 1;
+    if (j >= OUT) return;
+    float mu, var;
+    if (training) {
+        float cnt = 0.f, mean = 0.f, m2 = 0.f;
+        for (int bt = 0; bt < n_bt; ++bt) {
+            const float4 q = partials[(size_t)bt * OUT + j];
+            const float nab = cnt + q.x;
+            if (nab > 0.f) {
+                const float delta = q.y - mean;
+                const float fb = q.x / nab;
+                mean += delta * fb;
+                m2 += q.z + delta * delta * cnt * fb;
+                cnt = nab;
+            }
+        }
+        mu = mean;
+        var = fmaxf(m2 / (float)B, 0.f);
+        running_mean[j] = (1.f - momentum) * running_mean[j] + momentum * mu;
+        running_var[j] = (1.f - momentum) * running_var[j] +
+                         momentum * (m2 / (float)(B - 1));
+    } else {
+        mu = running_mean[j];
+        var = running_var[j];
+    }
+    const float inv = 1.0f / sqrtf(var + eps);
+    const float g = gamma ? gamma[j] : 1.f;
+    const float be = beta ? beta[j] : 0.f;
+    colp[j] = mu;
+    colp[OUT + j] = g * inv / divide_value;
+    colp[2 * OUT + j] = (be + add_bias[0]) / divide_value;
+}
+
+__device__ __forceinline__ float swish_f(float u) { return u / (1.0f + expf(-u)); }
+
+__global__ void normalize_swish_kernel(float* __restrict__ out, const float* __restrict__ colp,
+                                       int B, int OUT) {
+    const size_t total = (size_t)B * OUT;
+    if ((OUT & 3) == 0) {
+        float4* o4 = reinterpret_cast<float4*>(out);
+        for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total / 4;
+             i += (size_t)gridDim.x * blockDim.x) {
+            const int j = (int)((i * 4) % OUT);
+            const float4 c = *reinterpret_cast<const float4*>(colp + j);
+            const float4 s = *reinterpret_cast<const float4*>(colp + OUT + j);
+            const float4 h = *reinterpret_cast<const float4*>(colp + 2 * OUT + j);
+            float4 y = o4[i];
+            y.x = swish_f(fmaf(y.x - c.x, s.x, h.x));
+            y.y = swish_f(fmaf(y.y - c.y, s.y, h.y));
+            y.z = swish_f(fmaf(y.z - c.z, s.z, h.z));
+            y.w = swish_f(fmaf(y.w - c.w, s.w, h.w));
+            o4[i] = y;
+        }
+    } else {
+        for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+             i += (size_t)gridDim.x * blockDim.x) {
+            const int j = (int)(i % OUT);
+            out[i] = swish_f(fmaf(out[i] - colp[j], colp[OUT + j], colp[2 * OUT + j]));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+struct LinearPlan {
+    GemmPlan g;
+    int n_jt, n_bt;
+    size_t xpack_bytes, partials_off, colp_off, total;
+};
+
+static LinearPlan plan_linear(int B, int IN, int OUT) {
+    LinearPlan pl{};
+    const int BN = B <= 256 ? ((B + 15) / 16) * 16 : 256;
+    pl.n_bt = ceil_div(B, BN);
+    pl.n_jt = ceil_div(OUT, kBM);
+    const int n_kiters = ceil_div(IN, kBK);
+    const long long tiles = (long long)pl.n_jt * pl.n_bt;
+    pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), n_kiters, 2, 0);
+    pl.xpack_bytes = (size_t)pl.n_bt * n_kiters * 2 * BN * 128;
+    pl.partials_off = (pl.xpack_bytes + 255) & ~(size_t)255;
+    pl.colp_off = (pl.partials_off + (size_t)pl.n_bt * OUT * sizeof(float4) + 255) & ~(size_t)255;
+    pl.total = pl.colp_off + (size_t)3 * OUT * sizeof(float);
+    return pl;
+}
+
+}  // namespace nrc
+
+using namespace nrc;
+
+extern "C" size_t nrc_linear_bn_swish_workspace_size(int B, int in_f, int out_f) {
+    if (B <= 0 || in_f <= 0 || out_f <= 0) return 0;
+    return plan_linear(B, in_f, out_f).total;
+}
+
+extern "C" nrc_status nrc_linear_bn_swish(
+    const float* x, float* out, int B, int in_f, int out_f, const float* lin_weight,
+    const float* lin_bias, const float* bn_gamma, const float* bn_beta, float* bn_running_mean,
+    float* bn_running_var, int64_t* num_batches_tracked, float bn_eps, float bn_momentum,
+    int training, const float* add_bias, float divide_value, void* workspace,
+    size_t workspace_bytes, void* stream) {
+    if (!x || !out || !lin_weight || !bn_running_mean || !bn_running_var || !add_bias ||
+        !workspace)
+        return NRC_ERR_INVALID_ARG;
+    if (B <= 0 || in_f <= 0 || out_f <= 0) return NRC_ERR_INVALID_ARG;
+    if ((bn_gamma == nullptr) != (bn_beta == nullptr)) return NRC_ERR_INVALID_ARG;
+    if (!(bn_eps >= 0.f) || !std::isfinite(bn_eps)) return NRC_ERR_INVALID_ARG;
+    if (!(bn_momentum >= 0.f && bn_momentum <= 1.f)) return NRC_ERR_INVALID_ARG;
+    if (divide_value == 0.f || !std::isfinite(divide_value)) return NRC_ERR_INVALID_ARG;
+    if (training != 0 && training != 1) return NRC_ERR_INVALID_ARG;
+    if (training && B < 2) return NRC_ERR_UNSUPPORTED;
+    if (ranges_overlap(x, (size_t)B * in_f * 4, out, (size_t)B * out_f * 4))
+        return NRC_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return NRC_ERR_ALIGNMENT;
+    const LinearPlan pl = plan_linear(B, in_f, out_f);
+    if (workspace_bytes < pl.total) return NRC_ERR_WORKSPACE;
+    if ((long long)pl.n_jt * pl.n_bt >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    LinearParams p{};
+    p.W = lin_weight;
+    p.xpack = ws;
+    p.out = out;
+    p.lin_bias = lin_bias;
+    p.partials = reinterpret_cast<float4*>(ws + pl.partials_off);
+    p.B = B;
+    p.IN = in_f;
+    p.OUT = out_f;
+    p.n_jt = pl.n_jt;
+    p.n_bt = pl.n_bt;
+    p.n_kiters = pl.g.num_kiters;
+    p.BN = pl.g.BN;
+    p.vec_ok = (in_f % 4 == 0) && aligned(lin_weight, 16);
+    float* colp = reinterpret_cast<float*>(ws + pl.colp_off);
+
+    const size_t units = (size_t)pl.n_bt * pl.g.num_kiters * pl.g.BN * 8;
+    pack_rows_split_kernel<<<elementwise_grid(units), 256, 0, st>>>(x, ws, B, in_f, pl.g.BN,
+                                                                    pl.n_bt, pl.g.num_kiters);
+    if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
+    nrc_status s = launch_gemm<LinearProblem, 2>(p, pl.g, st);
+    if (s != NRC_OK) return s;
+    bn_finalize_kernel<<<ceil_div(out_f, 256), 256, 0, st>>>(
+        p.partials, pl.n_bt, B, out_f, bn_gamma, bn_beta, bn_running_mean, bn_running_var,
+        reinterpret_cast<long long*>(num_batches_tracked), bn_eps, bn_momentum, training,
+        add_bias, divide_value, colp);
+    if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
+    normalize_swish_kernel<<<elementwise_grid((size_t)B * out_f / 4 + 1), 256, 0, st>>>(
+        out, colp, B, out_f);
+    return cuda_status(cudaGetLastError());
+}

@@ -1,0 +1,32 @@
+// Host-side helpers shared by the translation units of libnrc.so.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/nrc.h"
+
+namespace nrc {
+
+// Device address of the status word (two ints) for the current device.
+int* device_status_ptr();
+// Current limit of every device-side wait (ns).
+unsigned long long wait_timeout_ns();
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+inline bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+inline bool aligned(const void* p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+inline nrc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NRC_OK : NRC_ERR_CUDA; }
+
+}  // namespace nrc

@@ -1,0 +1,134 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+function include/nrc.h declares; workspace queries; argument validation that
+returns before any CUDA call."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nrc.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and
+                                not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="needs nvcc to build libnrc.so")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from normalization_convolution_blocks_gb300 import api, build
+    build.build()
+    return api.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nrc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_blocks():
+    names = _declared_functions()
+    for n in ("nrc_prenorm_dilconv_residual", "nrc_conv1d_groupnorm", "nrc_linear_bn_swish"):
+        assert n in names
+
+
+def test_every_declared_function_is_exported(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    from normalization_convolution_blocks_gb300 import api
+    assert api.status_string(0) == "NRC_OK"
+    assert api.status_string(6) == "NRC_ERR_TIMEOUT"
+    assert api.status_string(99) == "NRC_ERR_UNKNOWN"
+
+
+def test_workspace_queries(lib):
+    from normalization_convolution_blocks_gb300 import api
+    # fp32 block: C=256 -> one 256-wide o tile, 12 K stages, hi+lo parts of 256 x 128 B
+    assert api.prenorm_dilconv_residual_workspace_size(256) == 12 * 2 * 256 * 128
+    assert api.prenorm_dilconv_residual_workspace_size(256, dtype=None) == 12 * 256 * 128
+    assert lib.nrc_prenorm_dilconv_residual_workspace_size(0, 0) == 0
+    assert api.conv1d_groupnorm_workspace_size(16, 128, 256, 1024, 32) > 0
+    assert api.linear_bn_swish_workspace_size(1024, 8192, 8192) > 2 * 1024 * 8192 * 2
+
+
+FAKE = ctypes.c_void_p(0x10000000)      # never dereferenced: validation fails first
+FAKE2 = ctypes.c_void_p(0x20000000)
+WS = ctypes.c_void_p(0x30000000)
+
+
+def _block(lib, **kw):
+    a = dict(x=FAKE, out=FAKE2, dt=0, N=2, C=32, L=64, k=3, d=4, pad=4, rm=FAKE, rv=FAKE,
+             g=FAKE, b=FAKE, eps=1e-5, w=FAKE, bias=FAKE, ws=WS, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.nrc_prenorm_dilconv_residual(a["x"], a["out"], a["dt"], a["N"], a["C"], a["L"],
+                                            a["k"], a["d"], a["pad"], a["rm"], a["rv"], a["g"],
+                                            a["b"], a["eps"], a["w"], a["bias"], a["ws"],
+                                            a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), 1), (dict(out=None), 1), (dict(rm=None), 1), (dict(w=None), 1),
+    (dict(ws=None), 1), (dict(N=0), 1), (dict(L=-1), 1), (dict(d=0, pad=0), 1),
+    (dict(dt=7), 1), (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
+    (dict(k=5), 2), (dict(pad=3), 2), (dict(C=4096), 2),
+    (dict(out=ctypes.c_void_p(0x10000000 + 64)), 1),          # out overlaps x
+    (dict(ws=ctypes.c_void_p(0x30000004)), 3),                 # misaligned workspace
+    (dict(wsb=16), 4),                                         # workspace too small
+])
+def test_block_validation(lib, kw, expect):
+    assert _block(lib, **kw) == expect
+
+
+def _gn(lib, **kw):
+    a = dict(x=FAKE, out=FAKE2, N=2, Cin=8, Cout=16, T=32, k=3, s=1, p=1, d=1, w=FAKE, bias=None,
+             G=4, g=FAKE, b=FAKE, eps=1e-5, ws=WS, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.nrc_conv1d_groupnorm(a["x"], a["out"], a["N"], a["Cin"], a["Cout"], a["T"],
+                                    a["k"], a["s"], a["p"], a["d"], a["w"], a["bias"], a["G"],
+                                    a["g"], a["b"], a["eps"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), 1), (dict(G=0), 1), (dict(G=3), 1), (dict(g=None), 1),
+    (dict(k=5), 2), (dict(s=2), 2), (dict(p=0), 2), (dict(d=2), 2),
+    (dict(Cout=768, G=64), 2),                                 # 12 channels/group, 768 > 256
+    (dict(wsb=8), 4), (dict(ws=ctypes.c_void_p(0x30000008)), 3),
+])
+def test_groupnorm_validation(lib, kw, expect):
+    assert _gn(lib, **kw) == expect
+
+
+def _lin(lib, **kw):
+    a = dict(x=FAKE, out=FAKE2, B=8, IN=16, OUT=16, w=FAKE, lb=None, g=None, b=None, rm=FAKE,
+             rv=FAKE, nbt=None, eps=1e-5, m=0.1, tr=1, ab=FAKE, div=1.0, ws=WS, wsb=1 << 30,
+             stream=None)
+    a.update(kw)
+    return lib.nrc_linear_bn_swish(a["x"], a["out"], a["B"], a["IN"], a["OUT"], a["w"], a["lb"],
+                                   a["g"], a["b"], a["rm"], a["rv"], a["nbt"], a["eps"], a["m"],
+                                   a["tr"], a["ab"], a["div"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), 1), (dict(ab=None), 1), (dict(rm=None), 1), (dict(g=FAKE), 1),
+    (dict(div=0.0), 1), (dict(m=1.5), 1), (dict(tr=2), 1), (dict(B=1), 2),
+    (dict(ws=ctypes.c_void_p(0x30000010)), 3), (dict(wsb=8), 4),
+])
+def test_linear_validation(lib, kw, expect):
+    assert _lin(lib, **kw) == expect
+
+
+def test_binding_fails_loudly_without_gpu():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from normalization_convolution_blocks_gb300 import api, synthetic
+    inp = synthetic.prenorm_block_inputs(1, 16, 32, 2)
+    with pytest.raises(RuntimeError):
+        api.prenorm_dilconv_residual(inp.x, inp.running_mean, inp.running_var, inp.gamma,
+                                     inp.beta, inp.eps, inp.weight, inp.bias, inp.dilation)

@@ -1,0 +1,115 @@
+"""GPU parity of nrc_prenorm_dilconv_residual against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from normalization_convolution_blocks_gb300 import synthetic as syn
+from gpu_util import assert_bf16, assert_f32, need_gpu, to
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(dev, inp, **kw):
+    from normalization_convolution_blocks_gb300 import api
+    w = kw.get("w", inp.weight)
+    b = kw.get("bias", inp.bias)
+    out = api.prenorm_dilconv_residual(to(dev, inp.x), to(dev, inp.running_mean),
+                                       to(dev, inp.running_var), to(dev, inp.gamma),
+                                       to(dev, inp.beta), inp.eps, to(dev, w), to(dev, b),
+                                       inp.dilation)
+    assert api.query_status() == api.NRC_OK
+    return out.double().cpu().numpy()
+
+
+def _oracle(inp, **kw):
+    return oracle.prenorm_block(inp.x, inp.running_mean, inp.running_var, inp.gamma, inp.beta,
+                                inp.eps, kw.get("w", inp.weight), kw.get("bias", inp.bias),
+                                inp.dilation)
+
+
+def test_tiny_workload_fp32():
+    dev = need_gpu()
+    inp = syn.WORKLOADS["prenorm_block_tiny_f32"].make(seed=0)
+    assert_f32(_gpu(dev, inp), _oracle(inp), "N2 C32 L512 d128")
+
+
+@pytest.mark.parametrize("N,C,L,d", [
+    (1, 16, 128, 1),        # one tile exactly
+    (2, 48, 300, 7),        # C not a multiple of 32, ragged L tail
+    (1, 64, 1000, 64),      # several tiles, ragged tail
+    (2, 256, 512, 128),     # full-width o tile
+    (1, 300, 260, 64),      # two o tiles, ragged channel count
+    (1, 96, 200, 150),      # dilation > L/2: side taps mostly padding
+    (1, 8, 5, 2),           # L smaller than a tile
+    (1, 1, 64, 3),          # single channel
+    (3, 80, 129, 128),      # tile + 1 row
+])
+def test_shapes_fp32(N, C, L, d):
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(N, C, L, d, seed=N * 1000 + C + d)
+    assert_f32(_gpu(dev, inp), _oracle(inp), f"N{N} C{C} L{L} d{d}")
+
+
+def test_no_bias():
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(2, 64, 256, 16, seed=5)
+    assert_f32(_gpu(dev, inp, bias=None), _oracle(inp, bias=None), "no bias")
+
+
+def test_zero_weights_reproduce_x_exactly():
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(2, 64, 300, 8, seed=6)
+    got = _gpu(dev, inp, w=torch.zeros_like(inp.weight), bias=torch.zeros_like(inp.bias))
+    assert np.array_equal(got, inp.x.double().numpy())
+
+
+def test_left_tap_identity_pins_padding_and_direction():
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(1, 32, 400, 37, seed=7)
+    C = 32
+    w = torch.zeros(C, C, 3)
+    w[torch.arange(C), torch.arange(C), 0] = 1.0
+    assert_f32(_gpu(dev, inp, w=w, bias=torch.zeros(C)), _oracle(inp, w=w, bias=torch.zeros(C)),
+               "left tap identity")
+
+
+@pytest.mark.parametrize("C,d", [(256, 1), (256, 8), (256, 128), (256, 512), (512, 128)])
+def test_bf16_storage(C, d):
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(2, C, 2048, d, seed=C + d, dtype=torch.bfloat16)
+    got = _gpu(dev, inp)
+    assert_bf16(got, _oracle(inp), f"bf16 C{C} d{d}")
+
+
+def test_full_workload_fp32_sampled_rows():
+    """The full-size workload (N=32 C=256 L=4096 d=128) in the bench's launch
+    configuration, compared on 48 sampled output rows (all L positions)."""
+    dev = need_gpu()
+    inp = syn.WORKLOADS["prenorm_block_f32"].make(seed=0)
+    got = _gpu(dev, inp)
+    rng = np.random.default_rng(0)
+    rn = np.concatenate([[0, 31, 31], rng.integers(0, 32, 45)])
+    ro = np.concatenate([[0, 255, 128], rng.integers(0, 256, 45)])
+    ref = oracle.prenorm_block_rows(inp.x, inp.running_mean, inp.running_var, inp.gamma,
+                                    inp.beta, inp.eps, inp.weight, inp.bias, inp.dilation, rn, ro)
+    assert_f32(got[rn, ro], ref, "full workload rows")
+
+
+@pytest.mark.parametrize("C,d", [(256, 1), (512, 512)])
+def test_full_bf16_workload_sampled_rows(C, d):
+    dev = need_gpu()
+    inp = syn.WORKLOADS[f"prenorm_block_bf16_C{C}_d{d}"].make(seed=0)
+    got = _gpu(dev, inp)
+    rng = np.random.default_rng(1)
+    rn, ro = rng.integers(0, 8, 24), rng.integers(0, C, 24)
+    ref = oracle.prenorm_block_rows(inp.x, inp.running_mean, inp.running_var, inp.gamma,
+                                    inp.beta, inp.eps, inp.weight, inp.bias, inp.dilation, rn, ro)
+    assert_bf16(got[rn, ro], ref, f"bf16 full C{C} d{d} rows")
+
+
+def test_repeat_calls_identical():
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(2, 128, 640, 32, seed=8)
+    a, b = _gpu(dev, inp), _gpu(dev, inp)
+    assert np.array_equal(a, b)

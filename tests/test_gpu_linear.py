@@ -1,0 +1,81 @@
+"""GPU parity of nrc_linear_bn_swish against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from normalization_convolution_blocks_gb300 import synthetic as syn
+from gpu_util import RUNNING_STAT_ABS, assert_f32, need_gpu, to
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(dev, li, training=True, nbt=None):
+    from normalization_convolution_blocks_gb300 import api
+    rm, rv = to(dev, li.running_mean).clone(), to(dev, li.running_var).clone()
+    out = api.linear_bn_swish(to(dev, li.x), to(dev, li.weight), to(dev, li.lin_bias),
+                              to(dev, li.gamma), to(dev, li.beta), rm, rv, to(dev, li.add_bias),
+                              li.divide_value, li.eps, li.momentum, training, nbt)
+    assert api.query_status() == api.NRC_OK
+    return out.double().cpu().numpy(), rm.double().cpu().numpy(), rv.double().cpu().numpy()
+
+
+def _ref(li, training=True, cols=None):
+    return oracle.linear_bn_swish(li.x, li.weight, li.lin_bias, li.gamma, li.beta,
+                                  li.running_mean, li.running_var, li.eps, li.momentum, training,
+                                  float(li.add_bias[0]), li.divide_value, cols=cols)
+
+
+def _check(got, ref, what):
+    out, rm, rv = got
+    r_out, r_rm, r_rv, _ = ref
+    assert_f32(out, r_out, what)
+    assert np.abs(rm - r_rm).max() < RUNNING_STAT_ABS, f"{what}: running_mean"
+    assert np.abs(rv - r_rv).max() < RUNNING_STAT_ABS, f"{what}: running_var"
+
+
+@pytest.mark.parametrize("B,IN,OUT,affine", [
+    (64, 256, 128, True), (64, 256, 128, False),
+    (100, 100, 70, True),     # ragged everywhere, in_features not a multiple of 4
+    (2, 64, 32, True),        # smallest training batch
+    (300, 520, 200, True),    # two batch tiles, ragged
+    (1024, 1024, 256, True),
+])
+def test_training_shapes(B, IN, OUT, affine):
+    dev = need_gpu()
+    li = syn.linear_bn_swish_inputs(B, IN, OUT, seed=B + IN + OUT, random_affine=affine)
+    _check(_gpu(dev, li), _ref(li), f"B{B} IN{IN} OUT{OUT}")
+
+
+def test_eval_mode_and_divide():
+    dev = need_gpu()
+    li = syn.linear_bn_swish_inputs(48, 160, 96, seed=4, random_affine=True)
+    g = torch.Generator().manual_seed(5)
+    li.running_mean = torch.randn(96, generator=g) * 0.1
+    li.running_var = torch.rand(96, generator=g) + 0.5
+    li.divide_value = 2.5
+    _check(_gpu(dev, li, training=False), _ref(li, training=False), "eval, divide 2.5")
+
+
+def test_num_batches_tracked_increments():
+    dev = need_gpu()
+    li = syn.linear_bn_swish_inputs(16, 32, 16, seed=6)
+    nbt = torch.zeros(1, dtype=torch.int64, device=dev)
+    _gpu(dev, li, nbt=nbt)
+    _gpu(dev, li, nbt=nbt)
+    assert int(nbt.item()) == 2
+    _gpu(dev, li, training=False, nbt=nbt)
+    assert int(nbt.item()) == 2
+
+
+def test_full_workload_sampled_columns():
+    """Full-size workload (1024 x 8192 -> 8192) in the bench's launch
+    configuration; 64 sampled columns (every batch row) and their running stats."""
+    dev = need_gpu()
+    li = syn.WORKLOADS["linear_bn_swish_f32"].make(seed=0)
+    out, rm, rv = _gpu(dev, li)
+    cols = np.concatenate([[0, 8191], np.random.default_rng(2).integers(0, 8192, 62)])
+    r_out, r_rm, r_rv, _ = _ref(li, cols=cols)
+    assert_f32(out[:, cols], r_out, "full workload columns")
+    assert np.abs(rm[cols] - r_rm[cols]).max() < RUNNING_STAT_ABS
+    assert np.abs(rv[cols] - r_rv[cols]).max() < RUNNING_STAT_ABS
