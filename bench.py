@@ -1,0 +1,561 @@
+#!/usr/bin/env python
+"""Benchmark of the normalization-fused Conv1d blocks on one GB300 per rank.
+
+Default workload: the full-size fp32 pre-norm residual block
+out = x + Conv1d(ReLU(BatchNorm1d_eval(x))), N=32 C=256 L=4096, k=3,
+dilation=padding=128 (x is 134 MB, 51.5 GFLOP per call).  One step = one call
+of the library's C ABI entry point (weight repack + fused implicit GEMM).
+
+Prints ONE JSON line (rank 0).  `value` is whole-job throughput in TFLOP/s of
+the block's algorithmic FLOPs (2*N*L*C_out*C_in*3) with inputs resident in
+HBM; `e2e` is the same metric through the public Python API with pinned host
+buffers (host->device copies of every input and the device->host copy of the
+output inside the timed region).  L2 is flushed (256 MB write, untimed)
+between timed steps.  Multi-GPU (torchrun) runs independent replicas: the
+blocks have no exchange step, so the work is weak-scaled with no collective
+on the data path; the barrier and the max-over-ranks timing use the process
+group only around the timed region.
+
+--impl reference times the fp64 CPU oracle (the checker of the library, not a
+tuned CPU implementation) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused norm+Conv1d block ms/call, TFLOP/s, % of roofline on 1 GB300"
+DEFAULT_WORKLOAD = "prenorm_block_f32"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TF32_PER_BF16 = 1.1 / 2.25        # nominal dense tf32 : bf16 tensor rate on GB300
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM traffic (read + write bytes) of one launch of the dominant kernel, from
+# one ncu capture (profiles/), keyed by workload; valid only while the kernel
+# sources hash to the recorded value.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "normalization_convolution_blocks_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Workload accounting
+# ---------------------------------------------------------------------------
+def workload_info(name):
+    """FLOPs and minimal bytes per call, dtype, and how the tensor peak is taken."""
+    from normalization_convolution_blocks_gb300 import synthetic as syn
+    wl = syn.WORKLOADS[name]
+    p = wl.params
+    if wl.kind == "block":
+        esz = 2 if p.get("dtype") == "bf16" else 4
+        N, C, L = p["N"], p["C"], p["L"]
+        flops = 2.0 * N * L * C * C * 3
+        min_bytes = esz * (2 * N * C * L + 3 * C * C + C) + 4 * 4 * C
+        cfg = dict(workload=name, N=N, C=C, L=L, kernel_size=3, dilation=p["dilation"],
+                   padding=p["dilation"], storage=p.get("dtype", "f32"))
+        dtype = "bf16" if esz == 2 else "f32"
+        main = "prenorm_block_gemm"
+    elif wl.kind == "conv_gn":
+        N, Cin, Cout, T = p["N"], p["Cin"], p["Cout"], p["T"]
+        flops = 2.0 * N * T * Cout * Cin * 3
+        min_bytes = 4 * (N * Cin * T + N * Cout * T + 3 * Cout * Cin + 2 * Cout)
+        cfg = dict(workload=name, N=N, C_in=Cin, C_out=Cout, T=T, kernel_size=3, padding=1,
+                   num_groups=p["G"], storage="f32")
+        dtype = "f32"
+        main = "conv_gn_gemm"
+    else:
+        B, IN, OUT = p["B"], p["IN"], p["OUT"]
+        flops = 2.0 * B * IN * OUT
+        min_bytes = 4 * (B * IN + OUT * IN + B * OUT + 5 * OUT)
+        cfg = dict(workload=name, B=B, in_features=IN, out_features=OUT, bn="training",
+                   storage="f32")
+        dtype = "f32"
+        main = "linear_gemm"
+    return dict(flops=flops, min_bytes=min_bytes, config=cfg, dtype=dtype, main_kernel=main,
+                kind=wl.kind)
+
+
+def roofline_peaks(info, peaks):
+    """Tensor peak of the contraction's own dtype: bf16 storage -> bf16; fp32
+    storage -> tf32 (the fp32 input type of the tensor cores), derived from the
+    measured bf16 peak by the nominal tf32:bf16 ratio."""
+    bf16 = peaks["bf16_tflops"]
+    if info["dtype"] == "bf16":
+        return bf16, "bf16 (measured burst)"
+    return bf16 * TF32_PER_BF16, "tf32 = measured bf16 burst x nominal 1.1/2.25"
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index):
+        self.proc = None
+        self.t0 = self.t1 = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            import torch
+            sel = []
+            try:
+                uuid = str(torch.cuda.get_device_properties(self.device_index).uuid)
+                sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+            except Exception:
+                pass
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"samples": 0, "note": "nvidia-smi unavailable"}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(row[0].strip().split(".")[0],
+                                               "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + row[0].strip().split(".")[1]) if "." in row[0] else 0.0
+                rows.append(dict(t=ts + frac, sm=float(row[1]), smax=float(row[2]),
+                                 power=float(row[3]) if row[3].strip() not in ("[N/A]", "") else None,
+                                 active=row[4].strip(),
+                                 hw=row[5].strip(), hwt=row[6].strip(), swt=row[7].strip(),
+                                 swp=row[8].strip()))
+            except (ValueError, IndexError):
+                continue
+        window = [r for r in rows if self.t0 is not None and self.t1 is not None
+                  and self.t0 - 0.15 <= r["t"] <= self.t1 + 0.15]
+        used = window if window else rows
+        if not used:
+            return {"samples": 0}
+        reasons = set()
+        for r in used:
+            for key, label in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                               ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(label)
+        return {"sm_mhz": statistics.median(r["sm"] for r in used),
+                "sm_max_mhz": max(r["smax"] for r in used),
+                "reasons": sorted(reasons),
+                "samples": len(used),
+                "in_window": bool(window),
+                "power_w_max": max((r["power"] for r in used if r["power"] is not None),
+                                   default=None)}
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas: barrier + max-over-ranks timing only)
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value, device=None):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# The GPU arm
+# ---------------------------------------------------------------------------
+def make_call(name, dev, host=False):
+    """Inputs of the workload (device-resident, or pinned host tensors) and a
+    closure running one call of the library on them."""
+    import torch
+
+    from normalization_convolution_blocks_gb300 import api
+    from normalization_convolution_blocks_gb300 import synthetic as syn
+    wl = syn.WORKLOADS[name]
+    inp = wl.make(seed=0)
+
+    def place(t):
+        if t is None:
+            return None
+        return t.pin_memory() if host else t.to(dev)
+
+    if wl.kind == "block":
+        x, rm, rv, g, b, w, bias = map(place, (inp.x, inp.running_mean, inp.running_var,
+                                              inp.gamma, inp.beta, inp.weight, inp.bias))
+        out = None if host else torch.empty_like(x)
+        ws = None if host else torch.empty(
+            api.prenorm_dilconv_residual_workspace_size(x.shape[1], x.dtype), dtype=torch.uint8,
+            device=dev)
+        tensors_in = (x, rm, rv, g, b, w, bias)
+
+        def call():
+            return api.prenorm_dilconv_residual(x, rm, rv, g, b, inp.eps, w, bias,
+                                                inp.dilation, out=out, workspace=ws)
+        out_shape = (x.shape, x.dtype)
+    elif wl.kind == "conv_gn":
+        x, w, g, b = map(place, (inp.x, inp.weight, inp.gamma, inp.beta))
+        N, Cin, T = x.shape
+        Cout = w.shape[0]
+        out = None if host else torch.empty((N, Cout, T), device=dev)
+        ws = None if host else torch.empty(
+            api.conv1d_groupnorm_workspace_size(N, Cin, Cout, T, inp.num_groups),
+            dtype=torch.uint8, device=dev)
+        tensors_in = (x, w, g, b)
+
+        def call():
+            return api.conv1d_groupnorm(x, w, None, inp.num_groups, g, b, inp.eps, out=out,
+                                        workspace=ws)
+        out_shape = ((N, Cout, T), torch.float32)
+    else:
+        x, w, lb, g, b, ab = map(place, (inp.x, inp.weight, inp.lin_bias, inp.gamma,
+                                         inp.beta, inp.add_bias))
+        rm, rv = inp.running_mean.to(dev), inp.running_var.to(dev)
+        nbt = torch.zeros(1, dtype=torch.int64, device=dev)
+        B, IN = x.shape
+        OUT = w.shape[0]
+        out = None if host else torch.empty((B, OUT), device=dev)
+        ws = None if host else torch.empty(api.linear_bn_swish_workspace_size(B, IN, OUT),
+                                           dtype=torch.uint8, device=dev)
+        tensors_in = (x, w, lb, g, b, ab)
+
+        def call():
+            return api.linear_bn_swish(x, w, lb, g, b, rm, rv, ab, inp.divide_value, inp.eps,
+                                       inp.momentum, True, nbt, out=out, workspace=ws)
+        out_shape = ((B, OUT), torch.float32)
+    h2d = sum(t.numel() * t.element_size() for t in tensors_in if t is not None)
+    d2h = math.prod(out_shape[0]) * (2 if out_shape[1] == torch.bfloat16 else 4)
+    return call, h2d, d2h
+
+
+def gpu_arm(args, world, rank, local):
+    import torch
+
+    from normalization_convolution_blocks_gb300 import api
+    from normalization_convolution_blocks_gb300 import build as nbuild
+    nbuild.build()
+    api.load()
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    info = workload_info(args.workload)
+    call, _, _ = make_call(args.workload, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        call()
+        flush.fill_(1.0)
+    torch.cuda.synchronize()
+    if api.query_status() != api.NRC_OK:
+        raise RuntimeError("device status error during warm-up")
+
+    steps = args.steps
+    if steps is None:   # aim at ~2 s of timed work so the clock sampler sees it
+        t0 = time.perf_counter()
+        for _ in range(5):
+            call()
+            flush.fill_(1.0)
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 5
+        steps = int(min(20000, max(20, 2.0 / max(per, 1e-6))))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    api.trace_enable(True)
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("begin")
+    for i in range(steps):
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+        flush.fill_(1.0)          # untimed: evict x/out/weights from L2 between steps
+    torch.cuda.synchronize()
+    barrier(world)
+    if sampler:
+        sampler.mark("end")
+    api.trace_enable(False)
+    clocks = sampler.stop() if sampler else None
+    if api.query_status() != api.NRC_OK:
+        raise RuntimeError("device status error in the timed region")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(world, sum(step_ms), dev)
+    recs = api.trace_records()
+    launches = len(recs)
+    per_kernel = {}
+    for name, ms in recs:
+        per_kernel.setdefault(name, []).append(ms)
+    main = info["main_kernel"]
+    main_ms = statistics.mean(per_kernel[main])
+
+    ms_per_step = total_ms / steps
+    value = world * info["flops"] / (ms_per_step * 1e-3) / 1e12
+    peaks, peaks_src = load_peaks()
+    tensor_peak, tensor_note = roofline_peaks(info, peaks)
+    hbm_peak = peaks["hbm_gbs"]
+    t_tensor = info["flops"] / (tensor_peak * 1e12)
+    t_hbm = info["min_bytes"] / (hbm_peak * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = info["flops"] / (main_ms * 1e-3) / 1e12
+        roof = dict(bound="tensor", achieved=round(achieved, 2), peak=round(tensor_peak, 1),
+                    unit="TFLOP/s", frac=round(achieved / tensor_peak, 4))
+    else:
+        achieved = info["min_bytes"] / (main_ms * 1e-3) / 1e9
+        roof = dict(bound="hbm", achieved=round(achieved, 1), peak=round(hbm_peak, 1),
+                    unit="GB/s", frac=round(achieved / hbm_peak, 4))
+    tr = NCU_TRAFFIC.get(args.workload)
+    roof["traffic"] = tr["bytes"] if tr and tr["src_hash"] == kernel_source_hash() else None
+    roof["kernel"] = main
+    roof["kernel_ms"] = round(main_ms, 5)
+    roof["peak_source"] = f"{peaks_src}: {tensor_note if roof['bound'] == 'tensor' else 'hbm_gbs'}"
+    roof["roofline_ms"] = round(max(t_tensor, t_hbm) * 1e3, 5)
+    if info["dtype"] == "f32":
+        # executed work: three bf16 products per term, against the bf16 peak
+        roof["executed_bf16_frac"] = round(3 * info["flops"] / (main_ms * 1e-3) / 1e12
+                                           / peaks["bf16_tflops"], 4)
+    kernels = {k: dict(launches=len(v), mean_ms=round(statistics.mean(v), 5),
+                       share=round(sum(v) / sum(sum(x) for x in per_kernel.values()), 4))
+               for k, v in per_kernel.items()}
+    result = dict(value=value, ms_per_step=ms_per_step, steps=steps, roofline=roof,
+                  launches=launches, kernels=kernels, clocks=clocks, info=info,
+                  step_ms_p10=sorted(step_ms)[len(step_ms) // 10],
+                  step_ms_p90=sorted(step_ms)[(9 * len(step_ms)) // 10])
+
+    # end to end through the public API with pinned host buffers
+    hcall, h2d, d2h = make_call(args.workload, dev, host=True)
+    hcall()
+    torch.cuda.synchronize()
+    n_e2e = max(3, min(steps, args.e2e_steps))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        hcall()                   # copies inputs in, runs, copies the output back (blocking)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_s = max_over_ranks(world, (time.perf_counter() - t0) / n_e2e, dev)
+    result["e2e"] = dict(value=world * info["flops"] / e2e_s / 1e12, unit="TFLOP/s",
+                         h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                         ms_per_step=e2e_s * 1e3, steps=n_e2e)
+    return result
+
+
+# ---------------------------------------------------------------------------
+# The oracle, timed on the host cores (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_sampler(name):
+    """Returns (run(n_units) -> flops done, unit description, total units)."""
+    import numpy as np
+
+    import oracle
+    from normalization_convolution_blocks_gb300 import synthetic as syn
+    wl = syn.WORKLOADS[name]
+    inp = wl.make(seed=0)
+    rng = np.random.default_rng(0)
+    if wl.kind == "block":
+        N, C, L = inp.x.shape
+        args = [t.double().numpy() for t in (inp.x, inp.running_mean, inp.running_var,
+                                             inp.gamma, inp.beta)]
+        w, b = inp.weight.double().numpy(), inp.bias.double().numpy()
+
+        def run(k):
+            rn, ro = rng.integers(0, N, k), rng.integers(0, C, k)
+            oracle.prenorm_block_rows(args[0], args[1], args[2], args[3], args[4], inp.eps, w, b,
+                                      inp.dilation, rn, ro)
+            return 2.0 * C * 3 * L * k
+        return run, "output rows (n, o, all L)", N * C
+    if wl.kind == "conv_gn":
+        N, Cin, T = inp.x.shape
+        Cout, G = inp.weight.shape[0], inp.num_groups
+        x, w = inp.x.double().numpy(), inp.weight.double().numpy()
+
+        def run(k):
+            oracle.conv_groupnorm_groups(x, w, None, G, inp.gamma, inp.beta, inp.eps,
+                                         rng.integers(0, N, k), rng.integers(0, G, k))
+            return 2.0 * (Cout // G) * T * Cin * 3 * k
+        return run, "GroupNorm groups (n, g)", N * G
+    B, IN = inp.x.shape
+    OUT = inp.weight.shape[0]
+    x, w = inp.x.double().numpy(), inp.weight.double().numpy()
+
+    def run(k):
+        oracle.linear_bn_swish(x, w, inp.lin_bias, inp.gamma, inp.beta, inp.running_mean,
+                               inp.running_var, inp.eps, inp.momentum, True,
+                               float(inp.add_bias[0]), inp.divide_value,
+                               cols=rng.integers(0, OUT, k))
+        return 2.0 * B * IN * k
+    return run, "output columns (all batch rows, BN over the batch)", OUT
+
+
+def size_sample(run, seconds):
+    """Units per sample so that one sample takes about `seconds`."""
+    k = 2
+    while True:
+        t0 = time.perf_counter()
+        run(k)
+        dt = time.perf_counter() - t0
+        if dt > 0.2 or k >= 1 << 20:
+            return max(1, int(k * seconds / max(dt, 1e-9)))
+        k *= 4
+
+
+def cpu_baseline(name, seconds=15.0):
+    import oracle
+    run, unit, total = oracle_sampler(name)
+    k = min(total, size_sample(run, seconds))
+    t0 = time.perf_counter()
+    flops = run(k)
+    dt = time.perf_counter() - t0
+    return dict(value=flops / dt / 1e12, unit="TFLOP/s", cores=oracle.max_threads(),
+                kind="oracle", sample=f"{k} of {total} {unit}, seed 0, {dt:.1f} s",
+                ms_per_call_equiv=dt * total / k * 1e3)
+
+
+def reference_arm(args):
+    import oracle
+    info = workload_info(args.workload)
+    run, unit, total = oracle_sampler(args.workload)
+    steps = args.steps if args.steps is not None else 5
+    budget = 150.0 / max(1, steps + args.warmup)       # whole run within a few minutes
+    k = min(total, size_sample(run, min(budget, 20.0)))
+    for _ in range(args.warmup):
+        run(k)
+    times, flops = [], 0.0
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        flops = run(k)
+        times.append(time.perf_counter() - t0)
+    per = statistics.mean(times)
+    value = flops / per / 1e12
+    sample = f"{k} of {total} {unit} per step, seed 0"
+    line = dict(impl="reference", metric=METRIC, value=value, unit="TFLOP/s", n_gpus=args.gpus,
+                steps=steps, warmup=args.warmup, ms_per_step=per * 1e3,
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic", config=dict(info["config"], l2="n/a (CPU)"),
+                cpu_baseline=dict(value=value, unit="TFLOP/s", cores=oracle.max_threads(),
+                                  kind="oracle", sample=sample),
+                e2e=dict(value=value, unit="TFLOP/s", h2d_bytes_per_step=0,
+                         d2h_bytes_per_step=0),
+                ms_per_call_equiv=per * total / k * 1e3)
+    return line
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_setup(args.gpus) if args.impl == "ours" else (
+        int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+
+    r = gpu_arm(args, world, rank, local)
+    if rank != 0:
+        return
+    info = r["info"]
+    line = dict(
+        metric=METRIC, value=round(r["value"], 3), unit="TFLOP/s", n_gpus=world,
+        steps=r["steps"], warmup=args.warmup, ms_per_step=round(r["ms_per_step"], 5),
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype=info["dtype"],
+        data="synthetic",
+        config=dict(info["config"], l2=f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB "
+                                        "write, untimed); x alone exceeds L2 on this workload",
+                    parallelism="replicas" if world > 1 else "single GPU",
+                    arithmetic=("bf16 tensor products, fp32 accumulate" if info["dtype"] == "bf16"
+                                else "3 bf16 tensor products per term (hi/lo split), "
+                                     "fp32 accumulate")),
+        roofline=r["roofline"], e2e=r["e2e"], gpu_launches=r["launches"],
+        clocks=r["clocks"],
+        ms_per_call_p10=round(r["step_ms_p10"], 5), ms_per_call_p90=round(r["step_ms_p90"], 5),
+        kernels=r["kernels"],
+    )
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -175,6 +175,21 @@ void nrc_set_wait_timeout_ns(uint64_t ns);
  * itself returns NRC_OK.  Read the outcome with nrc_query_status. */
 nrc_status nrc_selftest_wait_timeout(uint64_t limit_ns, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Launch trace (device timing of the library's own kernels)
+ * ------------------------------------------------------------------------ */
+/* on=1: drop earlier records and bracket every kernel launch made from now on
+ * with two CUDA events recorded on the launch's stream; on=0: stop recording
+ * (records are kept for reading). */
+void nrc_trace_enable(int on);
+
+/* Number of launches recorded since tracing was last enabled. */
+int nrc_trace_count(void);
+
+/* Record i: the kernel's name (static string) and its device duration in ms
+ * (waits for the record's end event). */
+nrc_status nrc_trace_get(int i, const char **name, float *ms);
+
 #ifdef __cplusplus
 }
 #endif

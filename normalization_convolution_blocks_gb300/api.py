@@ -61,6 +61,9 @@ def load() -> ctypes.CDLL:
         "nrc_last_error_site": ([], i),
         "nrc_set_wait_timeout_ns": ([u64], None),
         "nrc_selftest_wait_timeout": ([u64, p], i),
+        "nrc_trace_enable": ([i], None),
+        "nrc_trace_count": ([], i),
+        "nrc_trace_get": ([i, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(f)], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -268,3 +271,24 @@ def set_wait_timeout_ns(ns: int) -> None:
 def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     _check(load().nrc_selftest_wait_timeout(int(limit_ns), _stream(stream)),
            "nrc_selftest_wait_timeout")
+
+
+# ---------------------------------------------------------------------------
+# Launch trace
+# ---------------------------------------------------------------------------
+def trace_enable(on: bool = True) -> None:
+    """Start (clearing earlier records) or stop recording an event pair around
+    every kernel launch of the library."""
+    load().nrc_trace_enable(int(bool(on)))
+
+
+def trace_records():
+    """[(kernel name, device ms), ...] for the launches recorded so far."""
+    lib = load()
+    out = []
+    for i in range(lib.nrc_trace_count()):
+        name = ctypes.c_char_p()
+        ms = ctypes.c_float()
+        _check(lib.nrc_trace_get(i, ctypes.byref(name), ctypes.byref(ms)), "nrc_trace_get")
+        out.append((name.value.decode(), float(ms.value)))
+    return out

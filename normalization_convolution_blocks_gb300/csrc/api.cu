@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "nrc_host.h"
 #include "nrc_ptx.cuh"
@@ -52,6 +53,48 @@ int device_sm_count() {
         g_sm_count[d] = n > 0 ? n : 1;
     }
     return g_sm_count[d];
+}
+
+namespace {
+struct TraceRec {
+    const char* name;
+    cudaEvent_t start, stop;
+};
+std::mutex g_trace_mu;
+std::atomic<bool> g_trace_on{false};
+std::vector<TraceRec> g_trace;          // completed and open records
+std::vector<cudaEvent_t> g_event_pool;  // recycled events
+
+cudaEvent_t take_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+}  // namespace
+
+bool trace_enabled() { return g_trace_on.load(std::memory_order_relaxed); }
+
+void trace_record(const char* name, cudaStream_t s, bool begin) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (begin) {
+        TraceRec r{name, take_event(), nullptr};
+        cudaEventRecord(r.start, s);
+        g_trace.push_back(r);
+    } else {
+        // close the most recent open record of this name
+        for (auto it = g_trace.rbegin(); it != g_trace.rend(); ++it) {
+            if (it->name == name && it->stop == nullptr) {
+                it->stop = take_event();
+                cudaEventRecord(it->stop, s);
+                break;
+            }
+        }
+    }
 }
 
 // One thread waits, with a bounded limit, on an mbarrier that nothing arrives
@@ -114,4 +157,32 @@ extern "C" nrc_status nrc_selftest_wait_timeout(uint64_t limit_ns, void* stream)
     selftest_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
         status, (unsigned long long)limit_ns);
     return cuda_status(cudaGetLastError());
+}
+
+extern "C" void nrc_trace_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (on) {
+        for (auto& r : g_trace) {
+            if (r.start) g_event_pool.push_back(r.start);
+            if (r.stop) g_event_pool.push_back(r.stop);
+        }
+        g_trace.clear();
+    }
+    g_trace_on.store(on != 0);
+}
+
+extern "C" int nrc_trace_count(void) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    return (int)g_trace.size();
+}
+
+extern "C" nrc_status nrc_trace_get(int i, const char** name, float* ms) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (i < 0 || i >= (int)g_trace.size() || !name || !ms) return NRC_ERR_INVALID_ARG;
+    const TraceRec& r = g_trace[(size_t)i];
+    *name = r.name;
+    *ms = 0.f;
+    if (!r.stop) return NRC_ERR_INVALID_ARG;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess) return NRC_ERR_CUDA;
+    return cuda_status(cudaEventElapsedTime(ms, r.start, r.stop));
 }

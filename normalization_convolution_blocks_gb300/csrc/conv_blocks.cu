@@ -396,17 +396,25 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual(
     p.wpack = static_cast<const uint8_t*>(workspace);
     const size_t units = pl.wpack_bytes / 16 / NP;
     if (dt == NRC_F32) {
-        pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
-            static_cast<const float*>(conv_weight), static_cast<uint8_t*>(workspace), C, C,
-            pl.g.BN, pl.n_ot, pl.n_chunks);
+        {
+            TraceScope ts("pack_conv_weight", st);
+            pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
+                static_cast<const float*>(conv_weight), static_cast<uint8_t*>(workspace), C, C,
+                pl.g.BN, pl.n_ot, pl.n_chunks);
+        }
         if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
-        return launch_gemm<ConvProblem<float, ConvEpi::kResidual>, 2>(p, pl.g, st);
+        return launch_gemm<ConvProblem<float, ConvEpi::kResidual>, 2>("prenorm_block_gemm", p,
+                                                                      pl.g, st);
     }
-    pack_conv_weight_kernel<__nv_bfloat16, 1><<<elementwise_grid(units), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(conv_weight), static_cast<uint8_t*>(workspace), C, C,
-        pl.g.BN, pl.n_ot, pl.n_chunks);
+    {
+        TraceScope ts("pack_conv_weight", st);
+        pack_conv_weight_kernel<__nv_bfloat16, 1><<<elementwise_grid(units), 256, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(conv_weight), static_cast<uint8_t*>(workspace), C,
+            C, pl.g.BN, pl.n_ot, pl.n_chunks);
+    }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
-    return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual>, 1>(p, pl.g, st);
+    return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual>, 1>("prenorm_block_gemm",
+                                                                          p, pl.g, st);
 }
 
 static size_t gn_partials_offset(const ConvPlan& pl) {
@@ -467,12 +475,19 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     p.G = num_groups;
     p.cpg = cpg;
     const size_t units = pl.wpack_bytes / 16 / 2;
-    pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
-        conv_weight, ws, C_out, C_in, pl.g.BN, pl.n_ot, pl.n_chunks);
+    {
+        TraceScope ts("pack_conv_weight", st);
+        pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
+            conv_weight, ws, C_out, C_in, pl.g.BN, pl.n_ot, pl.n_chunks);
+    }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
-    nrc_status s = launch_gemm<ConvProblem<float, ConvEpi::kGroupStats>, 2>(p, pl.g, st);
+    nrc_status s =
+        launch_gemm<ConvProblem<float, ConvEpi::kGroupStats>, 2>("conv_gn_gemm", p, pl.g, st);
     if (s != NRC_OK) return s;
-    groupnorm_finalize_normalize_kernel<<<N * num_groups, 256, 0, st>>>(
-        out, p.partials, pl.n_tt * 4, C_out, T, num_groups, gn_gamma, gn_beta, eps);
+    {
+        TraceScope ts("groupnorm_finalize_normalize", st);
+        groupnorm_finalize_normalize_kernel<<<N * num_groups, 256, 0, st>>>(
+            out, p.partials, pl.n_tt * 4, C_out, T, num_groups, gn_gamma, gn_beta, eps);
+    }
     return cuda_status(cudaGetLastError());
 }

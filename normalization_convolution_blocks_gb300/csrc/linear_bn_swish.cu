@@ -282,17 +282,26 @@ extern "C" nrc_status nrc_linear_bn_swish(
     float* colp = reinterpret_cast<float*>(ws + pl.colp_off);
 
     const size_t units = (size_t)pl.n_bt * pl.g.num_kiters * pl.g.BN * 8;
-    pack_rows_split_kernel<<<elementwise_grid(units), 256, 0, st>>>(x, ws, B, in_f, pl.g.BN,
-                                                                    pl.n_bt, pl.g.num_kiters);
+    {
+        TraceScope ts("pack_rows_split", st);
+        pack_rows_split_kernel<<<elementwise_grid(units), 256, 0, st>>>(
+            x, ws, B, in_f, pl.g.BN, pl.n_bt, pl.g.num_kiters);
+    }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
-    nrc_status s = launch_gemm<LinearProblem, 2>(p, pl.g, st);
+    nrc_status s = launch_gemm<LinearProblem, 2>("linear_gemm", p, pl.g, st);
     if (s != NRC_OK) return s;
-    bn_finalize_kernel<<<ceil_div(out_f, 256), 256, 0, st>>>(
-        p.partials, pl.n_bt, B, out_f, bn_gamma, bn_beta, bn_running_mean, bn_running_var,
-        reinterpret_cast<long long*>(num_batches_tracked), bn_eps, bn_momentum, training,
-        add_bias, divide_value, colp);
+    {
+        TraceScope ts("bn_finalize", st);
+        bn_finalize_kernel<<<ceil_div(out_f, 256), 256, 0, st>>>(
+            p.partials, pl.n_bt, B, out_f, bn_gamma, bn_beta, bn_running_mean, bn_running_var,
+            reinterpret_cast<long long*>(num_batches_tracked), bn_eps, bn_momentum, training,
+            add_bias, divide_value, colp);
+    }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
-    normalize_swish_kernel<<<elementwise_grid((size_t)B * out_f / 4 + 1), 256, 0, st>>>(
-        out, colp, B, out_f);
+    {
+        TraceScope ts("normalize_swish", st);
+        normalize_swish_kernel<<<elementwise_grid((size_t)B * out_f / 4 + 1), 256, 0, st>>>(
+            out, colp, B, out_f);
+    }
     return cuda_status(cudaGetLastError());
 }

@@ -29,4 +29,22 @@ inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 inline nrc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NRC_OK : NRC_ERR_CUDA; }
 
+// Launch trace: when enabled (nrc_trace_enable), every kernel launch of the
+// library is bracketed by a pair of CUDA events recorded on its stream, so a
+// caller can read per-kernel device durations afterwards (nrc_trace_get).
+bool trace_enabled();
+void trace_record(const char* name, cudaStream_t s, bool begin);
+
+struct TraceScope {
+    const char* name;
+    cudaStream_t stream;
+    bool on;
+    TraceScope(const char* n, cudaStream_t s) : name(n), stream(s), on(trace_enabled()) {
+        if (on) trace_record(name, stream, true);
+    }
+    ~TraceScope() {
+        if (on) trace_record(name, stream, false);
+    }
+};
+
 }  // namespace nrc

@@ -32,8 +32,8 @@ inline GemmPlan make_gemm_plan(int BN, int num_tiles, int num_kiters, int NP,
 }
 
 template <class Prob, int NP>
-inline nrc_status launch_gemm(const typename Prob::Params& p, const GemmPlan& pl,
-                              cudaStream_t stream) {
+inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
+                              const GemmPlan& pl, cudaStream_t stream) {
     if (pl.stages < 2) return NRC_ERR_UNSUPPORTED;
     auto kern = gemm_kernel<Prob, NP>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -56,7 +56,10 @@ inline nrc_status launch_gemm(const typename Prob::Params& p, const GemmPlan& pl
     // Co-resident CTAs must also fit their TMEM allocations (512 columns per SM).
     per_sm = std::max(1, std::min(per_sm, (int)(512u / cfg.tmem_cols)));
     const int grid = std::min(pl.num_tiles, device_sm_count() * per_sm);
-    kern<<<grid, kThreads, pl.smem_bytes, stream>>>(p, cfg);
+    {
+        TraceScope ts(name, stream);
+        kern<<<grid, kThreads, pl.smem_bytes, stream>>>(p, cfg);
+    }
     return cuda_status(cudaGetLastError());
 }
 
