@@ -94,11 +94,16 @@ __device__ __forceinline__ void warp_merge_stats(float& cnt, float& mean, float&
 template <typename T, ConvEpi EPI>
 struct ConvProblem {
     using Params = ConvParams;
+    using Tile = ConvTile;
+
+    static __device__ __forceinline__ Tile tile_info(const Params& p, int tile) {
+        return conv_tile(p, tile);
+    }
 
     static __device__ void setup(const Params& p, uint8_t* extra) {
         if (p.rm == nullptr) return;
         // BN fold: z = max(0, x*scale + shift), scale = gamma/sqrt(rv+eps),
-        // shift = beta - rm*scale.  Channels past Cin get 0 (never used: guarded).
+        // shift = beta - rm*scale.  Channels past Cin get 0.
         float* sc = reinterpret_cast<float*>(extra);
         float* sh = sc + p.n_chunks * kBK;
         for (int c = threadIdx.x; c < p.n_chunks * kBK; c += blockDim.x) {
@@ -112,43 +117,63 @@ struct ConvProblem {
         }
     }
 
-    static __device__ __forceinline__ void fetch_a(const Params& p, const uint8_t* extra,
-                                                   int tile, int kiter, int row, int k0,
-                                                   float (&v)[32]) {
-        const ConvTile tl = conv_tile(p, tile);
-        const int tap = kiter / p.n_chunks;
+    // Input position read by tap `tap` for output row t, and the channel base.
+    static __device__ __forceinline__ void where(const Params& p, const Tile& tl, int kiter,
+                                                 int row, int k0, int& s, int& c0) {
+        const int tap = kiter >= 2 * p.n_chunks ? 2 : (kiter >= p.n_chunks ? 1 : 0);
         const int chunk = kiter - tap * p.n_chunks;
-        const int t = tl.tt * kBM + row;
-        const int s = t - p.pad + tap * p.dil;
-        const bool s_ok = (unsigned)s < (unsigned)p.L;
-        const int c0 = chunk * kBK + k0;
-        const T* xp = static_cast<const T*>(p.x) + ((size_t)tl.n * p.Cin + c0) * p.L + s;
-        float raw[32];
+        s = tl.tt * kBM + row - p.pad + tap * p.dil;
+        c0 = chunk * kBK + k0;
+    }
+
+    static __device__ __forceinline__ void load_a(const Params& p, const Tile& tl, int kiter,
+                                                  int row, int k0, float (&v)[32]) {
+        int s, c0;
+        where(p, tl, kiter, row, k0, s, c0);
+        if ((unsigned)s < (unsigned)p.L) {
+            const T* xp = static_cast<const T*>(p.x) + ((size_t)tl.n * p.Cin + c0) * p.L + s;
+            if (c0 + 32 <= p.Cin) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            raw[i] = (s_ok && c0 + i < p.Cin) ? load_f<T>(xp + (size_t)i * p.L) : 0.f;
-        if (p.rm != nullptr) {
-            const float* sc = reinterpret_cast<const float*>(extra) + c0;
-            const float* sh = reinterpret_cast<const float*>(extra) + p.n_chunks * kBK + c0;
+                for (int i = 0; i < 32; ++i) v[i] = load_f<T>(xp + (size_t)i * p.L);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)   // zero padding applies to z, after BN+ReLU
-                v[i] = s_ok ? fmaxf(fmaf(raw[i], sc[i], sh[i]), 0.f) : 0.f;
+                for (int i = 0; i < 32; ++i)
+                    v[i] = (c0 + i < p.Cin) ? load_f<T>(xp + (size_t)i * p.L) : 0.f;
+            }
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = raw[i];
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;   // zero padding of the conv input
         }
     }
 
-    static __device__ __forceinline__ const void* b_src(const Params& p, int tile, int kiter) {
-        const int ot = tile % p.n_ot;
-        constexpr int NP = sizeof(T) == 4 ? 2 : 1;
-        return p.wpack + ((size_t)ot * p.n_kiters + kiter) * NP * (size_t)p.BN * 128u;
+    static __device__ __forceinline__ void finish_a(const Params& p, const uint8_t* extra,
+                                                    const Tile& tl, int kiter, int row, int k0,
+                                                    float (&v)[32]) {
+        if (p.rm == nullptr) return;                   // plain conv input
+        int s, c0;
+        where(p, tl, kiter, row, k0, s, c0);
+        if ((unsigned)s >= (unsigned)p.L) return;      // padding applies to z, after BN+ReLU
+        const float4* sc = reinterpret_cast<const float4*>(extra) + c0 / 4;
+        const float4* sh = reinterpret_cast<const float4*>(extra) + (p.n_chunks * kBK + c0) / 4;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 a = sc[q], b = sh[q];
+            v[4 * q] = fmaxf(fmaf(v[4 * q], a.x, b.x), 0.f);
+            v[4 * q + 1] = fmaxf(fmaf(v[4 * q + 1], a.y, b.y), 0.f);
+            v[4 * q + 2] = fmaxf(fmaf(v[4 * q + 2], a.z, b.z), 0.f);
+            v[4 * q + 3] = fmaxf(fmaf(v[4 * q + 3], a.w, b.w), 0.f);
+        }
     }
 
-    static __device__ __forceinline__ void epilogue(const Params& p, const uint8_t*, int tile,
-                                                    int quarter, int lane, uint32_t taddr,
-                                                    int BN) {
-        const ConvTile tl = conv_tile(p, tile);
+    static __device__ __forceinline__ const void* b_src(const Params& p, const Tile& tl,
+                                                        int kiter) {
+        constexpr int NP = sizeof(T) == 4 ? 2 : 1;
+        return p.wpack + ((size_t)tl.ot * p.n_kiters + kiter) * NP * (size_t)p.BN * 128u;
+    }
+
+    static __device__ __forceinline__ void epilogue(const Params& p, const uint8_t*,
+                                                    const Tile& tl, int quarter, int lane,
+                                                    uint32_t taddr, int BN) {
         const int t = tl.tt * kBM + quarter * 32 + lane;
         const bool t_ok = t < p.L;
         const T* bias = static_cast<const T*>(p.bias);
@@ -157,12 +182,22 @@ struct ConvProblem {
         const size_t row0 = (size_t)tl.n * p.Cout;
         if constexpr (EPI == ConvEpi::kResidual) {
             const T* x = static_cast<const T*>(p.x);
-            for (int cc = 0; cc < BN; cc += 16) {
-                float r[16];
+            // residual of the next 16 channels is loaded one chunk ahead
+            float r[16], rn[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int o = obase + cc + i;
-                    r[i] = (t_ok && o < p.Cout) ? load_f<T>(x + (row0 + o) * p.L + t) : 0.f;
+            for (int i = 0; i < 16; ++i) {
+                const int o = obase + i;
+                rn[i] = (t_ok && o < p.Cout) ? load_f<T>(x + (row0 + o) * p.L + t) : 0.f;
+            }
+            for (int cc = 0; cc < BN; cc += 16) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = rn[i];
+                if (cc + 16 < BN) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int o = obase + cc + 16 + i;
+                        rn[i] = (t_ok && o < p.Cout) ? load_f<T>(x + (row0 + o) * p.L + t) : 0.f;
+                    }
                 }
                 float v[16];
                 tmem_ld16(taddr + (uint32_t)cc, v);
@@ -183,8 +218,7 @@ struct ConvProblem {
                 tmem_ld16(taddr + (uint32_t)cc, v);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int col = cc + i;
-                    const int o = obase + col;
+                    const int o = obase + cc + i;
                     if (o >= p.Cout) break;                 // uniform across the warp
                     const float y = v[i] + (bias ? load_f<T>(bias + o) : 0.f);
                     if (t_ok) {

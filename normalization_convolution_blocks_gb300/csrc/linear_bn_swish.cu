@@ -32,16 +32,25 @@ struct LinearParams {
     int vec_ok;              // W 16-byte aligned and IN % 4 == 0
 };
 
+struct LinearTile {
+    int jt, bt;
+};
+
 struct LinearProblem {
     using Params = LinearParams;
+    using Tile = LinearTile;
+
+    // Tiles of one feature block are adjacent, so the CTAs reading the same
+    // weight rows run together and the weight is fetched from HBM once.
+    static __device__ __forceinline__ Tile tile_info(const Params& p, int tile) {
+        return Tile{tile / p.n_bt, tile % p.n_bt};
+    }
 
     static __device__ void setup(const Params&, uint8_t*) {}
 
-    static __device__ __forceinline__ void fetch_a(const Params& p, const uint8_t*, int tile,
-                                                   int kiter, int row, int k0,
-                                                   float (&v)[32]) {
-        const int jt = tile / p.n_bt;
-        const int j = jt * kBM + row;
+    static __device__ __forceinline__ void load_a(const Params& p, const Tile& tl, int kiter,
+                                                  int row, int k0, float (&v)[32]) {
+        const int j = tl.jt * kBM + row;
         const int k = kiter * kBK + k0;
         if (j >= p.OUT) {
 #pragma unroll
@@ -65,19 +74,21 @@ struct LinearProblem {
         }
     }
 
-    static __device__ __forceinline__ const void* b_src(const Params& p, int tile, int kiter) {
-        const int bt = tile % p.n_bt;
-        return p.xpack + ((size_t)bt * p.n_kiters + kiter) * 2 * (size_t)p.BN * 128u;
+    static __device__ __forceinline__ void finish_a(const Params&, const uint8_t*, const Tile&,
+                                                    int, int, int, float (&)[32]) {}
+
+    static __device__ __forceinline__ const void* b_src(const Params& p, const Tile& tl,
+                                                        int kiter) {
+        return p.xpack + ((size_t)tl.bt * p.n_kiters + kiter) * 2 * (size_t)p.BN * 128u;
     }
 
-    static __device__ __forceinline__ void epilogue(const Params& p, const uint8_t*, int tile,
-                                                    int quarter, int lane, uint32_t taddr,
-                                                    int BN) {
-        const int jt = tile / p.n_bt, bt = tile % p.n_bt;
-        const int j = jt * kBM + quarter * 32 + lane;
+    static __device__ __forceinline__ void epilogue(const Params& p, const uint8_t*,
+                                                    const Tile& tl, int quarter, int lane,
+                                                    uint32_t taddr, int BN) {
+        const int j = tl.jt * kBM + quarter * 32 + lane;
         const bool j_ok = j < p.OUT;
         const float lb = (j_ok && p.lin_bias) ? __ldg(p.lin_bias + j) : 0.f;
-        const int b0 = bt * BN;
+        const int b0 = tl.bt * BN;
         float cnt = 0.f, mean = 0.f, m2 = 0.f;
         for (int cc = 0; cc < BN; cc += 16) {
             float v[16];
@@ -95,7 +106,7 @@ struct LinearProblem {
                 }
             }
         }
-        if (j_ok) p.partials[(size_t)bt * p.OUT + j] = make_float4(cnt, mean, m2, 0.f);
+        if (j_ok) p.partials[(size_t)tl.bt * p.OUT + j] = make_float4(cnt, mean, m2, 0.f);
     }
 };
 

@@ -1,19 +1,30 @@
 // Persistent, warp-specialized tcgen05 GEMM skeleton shared by the three
 // blocks.  One CTA per SM walks a static round-robin list of 128 x BN output
-// tiles; D = A * B^T with A (128 x K) produced in shared memory by eight
-// "prologue" warps (each block's own load-and-transform), B (BN x K) bulk-copied
-// from a pre-packed global image, and the fp32 accumulator in TMEM (two
-// buffers, so the epilogue of one tile overlaps the mainloop of the next).
+// tiles and computes D[128 x BN] = A[128 x K] * B[BN x K]^T:
+//
+//   * A (the activation side) is produced by eight prologue warps: each block's
+//     own load-and-transform, split into bf16 parts and written straight into
+//     tensor memory with tcgen05.st; the MMA reads A from TMEM.
+//   * B (the weight side) is bulk-copied (cp.async.bulk) from a pre-packed
+//     global image into a ring of shared-memory stages in the 128-byte swizzle
+//     layout the MMA's shared-memory descriptor expects.
+//   * The fp32 accumulator lives in TMEM; the epilogue warps drain it.
+//
+// Keeping A out of shared memory leaves shared-memory bandwidth to the weight
+// stream alone, which the MMAs read at 64 B/clk at full rate.
 //
 // fp32 storage runs three bf16 MMAs per K step (hi*hi + lo*hi + hi*lo, with
 // v = hi + lo split in bf16): products exact to ~2^-16 relative, accumulated in
-// fp32 on the tensor cores.  bf16 storage runs one.
+// fp32.  bf16 storage runs one.
 //
 // Warp roles (448 threads):
-//   warp 0      B producer: one thread issues cp.async.bulk per stage
-//   warp 1      TMEM allocator; one thread issues tcgen05.mma and commits
-//   warps 2-9   A producers: warp w writes rows 32*(w%4).. of the stage, K half (w-2)/4
-//   warps 10-13 epilogue: warp w drains TMEM lanes 32*(w%4).. (its lane quarter)
+//   warp 0      B producer: one thread issues the bulk copies
+//   warp 1      allocates all 512 TMEM columns; one thread issues the MMAs
+//   warps 2-9   A producers: warp w owns TMEM lanes 32*(w%4).. (tile rows), K half (w-2)/4
+//   warps 10-13 epilogue: warp w drains TMEM lanes 32*(w%4)..
+//
+// TMEM columns: [0, BN) accumulator; [256, 512) A ring, stage s at
+// 256 + s*32*NP (hi part: 32 columns = 64 bf16 of K; then the lo part).
 #pragma once
 #include <cstdint>
 
@@ -25,9 +36,10 @@ constexpr int kThreads = 448;
 constexpr int kBM = 128;            // rows of a tile (MMA M)
 constexpr int kBK = 64;             // K elements per stage (one 128-byte swizzle row)
 constexpr int kUMMA_K = 16;         // K of one bf16 MMA
-constexpr uint32_t kATileBytes = kBM * 128;   // one bf16 part of an A stage
 constexpr int kMaxStages = 8;
 constexpr int kMaxSmemBytes = 232448;          // 227 KB opt-in per CTA
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemARing = 256;           // first column of the A ring
 
 enum WaitSite : int {
     kSiteBEmpty = 1, kSiteAEmpty = 2, kSiteAccEmpty = 3, kSiteFullA = 4, kSiteFullB = 5,
@@ -38,86 +50,101 @@ struct GemmCfg {
     int BN;                 // tile columns (multiple of 16, <= 256)
     int num_tiles;
     int num_kiters;         // K stages per tile
-    int stages;             // pipeline depth
-    uint32_t stage_bytes;   // NP * (kATileBytes + BN * 128)
-    uint32_t tmem_cols;     // power of two >= 2 * BN
+    int b_stages;           // depth of the shared-memory B ring
+    uint32_t b_stage_bytes; // NP * BN * 128
     int* status;            // device status word
     unsigned long long timeout_ns;
 };
 
-// Shared-memory footprint of the skeleton's bookkeeping after the stages.
-__host__ __device__ constexpr uint32_t gemm_bookkeeping_bytes(int stages) {
-    return (uint32_t)(3 * stages + 5) * 8u + 16u;
+// Shared-memory bookkeeping after the B stages: barriers and two words.
+__host__ __device__ constexpr uint32_t gemm_bookkeeping_bytes() {
+    return (((uint32_t)(4 * kMaxStages + 5) * 8u + 16u) + 63u) & ~63u;
 }
 
 template <int NP>
-__host__ __device__ constexpr uint32_t gemm_stage_bytes(int BN) {
-    return (uint32_t)NP * (kATileBytes + (uint32_t)BN * 128u);
+__device__ __forceinline__ void split_store_a(uint32_t taddr_hi, const float (&v)[32]) {
+    uint32_t h[16];
+    if constexpr (NP == 2) {
+        uint32_t l[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) split_bf16x2(v[2 * e], v[2 * e + 1], h[e], l[e]);
+        tmem_st16(taddr_hi, h);
+        tmem_st16(taddr_hi + 32u, l);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) h[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+        tmem_st16(taddr_hi, h);
+    }
 }
 
 // Prob must provide:
-//   struct Params;
-//   static constexpr uint32_t extra_smem_bytes(const Params&)   [host]
-//   static __device__ void setup(const Params&, uint8_t* extra)         (all threads)
-//   static __device__ void fetch_a(const Params&, const uint8_t* extra, int tile,
-//                                  int kiter, int row, int k0, float (&v)[32])
-//        -> the 32 fp32 values A[row][kiter*64 + k0 .. +32) after the block's transform
-//   static __device__ const void* b_src(const Params&, int tile, int kiter)
+//   struct Params; struct Tile;
+//   static __device__ Tile tile_info(const Params&, int tile)
+//   static __device__ void setup(const Params&, uint8_t* extra)        (all threads)
+//   static __device__ void load_a(const Params&, const Tile&, int kiter, int row, int k0,
+//                                 float (&v)[32])
+//        -> issues the loads of the raw values A[row][kiter*64 + k0 .. +32)
+//   static __device__ void finish_a(const Params&, const uint8_t* extra, const Tile&,
+//                                   int kiter, int row, int k0, float (&v)[32])
+//        -> the block's transform, in place (runs after the loads have landed)
+//   static __device__ const void* b_src(const Params&, const Tile&, int kiter)
 //        -> packed B image of the stage: NP parts of BN rows x 128 B, swizzled
-//   static __device__ void epilogue(const Params&, const uint8_t* extra, int tile, int quarter,
-//                                   int lane, uint32_t taddr, int BN)
-//        -> drains TMEM columns [taddr, taddr + BN) of its lane quarter (all lanes
-//           execute the tcgen05.ld calls)
+//   static __device__ void epilogue(const Params&, const uint8_t* extra, const Tile&,
+//                                   int quarter, int lane, uint32_t taddr, int BN)
+//        -> drains TMEM columns [taddr, taddr + BN) of its lane quarter (every lane
+//           executes the tcgen05.ld calls)
 template <class Prob, int NP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const typename Prob::Params p, const GemmCfg cfg) {
+    using Tile = typename Prob::Tile;
+    constexpr int SA = (int)((kTmemCols - kTmemARing) / (32u * NP));   // A ring depth
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int S = cfg.stages;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * cfg.stage_bytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
+    const int SB = cfg.b_stages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)SB * cfg.b_stage_bytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * kMaxStages + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    uint8_t* extra = reinterpret_cast<uint8_t*>(tmem_slot + 4);
+    uint8_t* extra = reinterpret_cast<uint8_t*>(smem) + (size_t)SB * cfg.b_stage_bytes +
+                     gemm_bookkeeping_bytes();
 
     const uint32_t bar0 = smem_u32(bars);
-    auto full_a = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-    auto full_b = [&](int s) { return bar0 + 8u * (uint32_t)(S + s); };
-    auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(2 * S + s); };
-    auto acc_full = [&](int a) { return bar0 + 8u * (uint32_t)(3 * S + a); };
-    auto acc_empty = [&](int a) { return bar0 + 8u * (uint32_t)(3 * S + 2 + a); };
-    const uint32_t drain_bar = bar0 + 8u * (uint32_t)(3 * S + 4);
+    auto a_full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+    auto a_empty = [&](int s) { return bar0 + 8u * (uint32_t)(kMaxStages + s); };
+    auto b_full = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kMaxStages + s); };
+    auto b_empty = [&](int s) { return bar0 + 8u * (uint32_t)(3 * kMaxStages + s); };
+    const uint32_t acc_full = bar0 + 8u * (uint32_t)(4 * kMaxStages);
+    const uint32_t acc_empty = acc_full + 8u;
+    const uint32_t drain_bar = acc_full + 16u;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BN = cfg.BN;
-    const uint32_t b_bytes = (uint32_t)NP * (uint32_t)BN * 128u;
     WaitCtx ctx{abort_flag, cfg.status, cfg.timeout_ns};
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full_a(s), 8);      // one arrival per A-producer warp
-            mbar_init(full_b(s), 1);      // producer's arrive.expect_tx
-            mbar_init(empty(s), 1);       // MMA commit
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(a_full(s), 8);      // one arrival per A-producer warp
+            mbar_init(a_empty(s), 1);     // MMA commit
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(acc_full(a), 1);    // MMA commit
-            mbar_init(acc_empty(a), 4);   // one arrival per epilogue warp
+        for (int s = 0; s < SB; ++s) {
+            mbar_init(b_full(s), 1);      // producer's arrive.expect_tx
+            mbar_init(b_empty(s), 1);     // MMA commit
         }
+        mbar_init(acc_full, 1);           // MMA commit
+        mbar_init(acc_empty, 4);          // one arrival per epilogue warp
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     Prob::setup(p, extra);
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), cfg.tmem_cols);
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-
-    auto stage_ptr = [&](int s) { return smem + (size_t)s * cfg.stage_bytes; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ B producer
@@ -129,70 +156,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kMaxStages; ++s) armed[s] = false;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < cfg.num_tiles; tile += gridDim.x) {
+                const Tile tl = Prob::tile_info(p, tile);
                 for (int k = 0; k < cfg.num_kiters; ++k) {
-                    if (!mbar_wait(empty(stage), phase ^ 1u, ctx, kSiteBEmpty)) {
+                    if (!mbar_wait(b_empty(stage), phase ^ 1u, ctx, kSiteBEmpty)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_b(stage), b_bytes);
-                    bulk_g2s(smem_u32(stage_ptr(stage) + NP * kATileBytes),
-                             Prob::b_src(p, tile, k), b_bytes, full_b(stage));
+                    mbar_arrive_expect_tx(b_full(stage), cfg.b_stage_bytes);
+                    bulk_g2s(smem_u32(smem + (size_t)stage * cfg.b_stage_bytes),
+                             Prob::b_src(p, tl, k), cfg.b_stage_bytes, b_full(stage));
                     armed[stage] = true;
                     armed_parity[stage] = phase;
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                    if (++stage == SB) { stage = 0; phase ^= 1u; }
                 }
             }
             if (!ok) {
                 // Let every copy still in flight land before the CTA can exit.
-                for (int s = 0; s < S; ++s)
-                    if (armed[s]) mbar_wait_drain(full_b(s), armed_parity[s], 200000000ull);
+                for (int s = 0; s < SB; ++s)
+                    if (armed[s]) mbar_wait_drain(b_full(s), armed_parity[s], 200000000ull);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kBM, BN);
-            int stage = 0;
-            uint32_t phase = 0;
+            int sa = 0, sb = 0;
+            uint32_t pha = 0, phb = 0;
             bool ok = true;
             int it = 0;
             for (int tile = blockIdx.x; ok && tile < cfg.num_tiles; tile += gridDim.x, ++it) {
-                const int acc = it & 1;
-                const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-                if (!mbar_wait(acc_empty(acc), acc_phase ^ 1u, ctx, kSiteAccEmpty)) {
+                if (!mbar_wait(acc_empty, ((uint32_t)it & 1u) ^ 1u, ctx, kSiteAccEmpty)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int k = 0; k < cfg.num_kiters; ++k) {
-                    if (!mbar_wait(full_a(stage), phase, ctx, kSiteFullA) ||
-                        !mbar_wait(full_b(stage), phase, ctx, kSiteFullB)) {
+                    if (!mbar_wait(a_full(sa), pha, ctx, kSiteFullA) ||
+                        !mbar_wait(b_full(sb), phb, ctx, kSiteFullB)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_hi = smem_u32(stage_ptr(stage));
-                    const uint32_t b_hi = a_hi + NP * kATileBytes;
+                    const uint32_t a_col = tmem_base + kTmemARing + (uint32_t)(sa * 32 * NP);
+                    const uint32_t b_hi = smem_u32(smem + (size_t)sb * cfg.b_stage_bytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / kUMMA_K; ++kk) {
-                        const uint32_t koff = (uint32_t)kk * (kUMMA_K * 2);
-                        const uint64_t ad = sw128_kmajor_desc(a_hi + koff);
-                        const uint64_t bd = sw128_kmajor_desc(b_hi + koff);
-                        mma_bf16_ss(d_tmem, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+                        const uint32_t a_k = a_col + (uint32_t)(kk * kUMMA_K / 2);
+                        const uint64_t bd = sw128_kmajor_desc(b_hi + (uint32_t)kk * (kUMMA_K * 2));
+                        mma_bf16_ts(tmem_base, a_k, bd, idesc, (k | kk) != 0 ? 1u : 0u);
                         if constexpr (NP == 2) {
-                            const uint64_t ad_lo = sw128_kmajor_desc(a_hi + kATileBytes + koff);
-                            const uint64_t bd_lo =
-                                sw128_kmajor_desc(b_hi + (uint32_t)BN * 128u + koff);
-                            mma_bf16_ss(d_tmem, ad_lo, bd, idesc, 1u);
-                            mma_bf16_ss(d_tmem, ad, bd_lo, idesc, 1u);
+                            const uint64_t bd_lo = sw128_kmajor_desc(
+                                b_hi + (uint32_t)BN * 128u + (uint32_t)kk * (kUMMA_K * 2));
+                            mma_bf16_ts(tmem_base, a_k + 32u, bd, idesc, 1u);   // lo * hi
+                            mma_bf16_ts(tmem_base, a_k, bd_lo, idesc, 1u);      // hi * lo
                         }
                     }
-                    mma_commit(empty(stage));          // stage free once these MMAs finish
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                    mma_commit(a_empty(sa));           // A stage free once these finish
+                    mma_commit(b_empty(sb));           // B stage likewise
+                    if (++sa == SA) { sa = 0; pha ^= 1u; }
+                    if (++sb == SB) { sb = 0; phb ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit(acc_full(acc));             // accumulator ready for the epilogue
+                mma_commit(acc_full);                  // accumulator ready for the epilogue
             }
             if (!ok) {
                 // Every MMA issued so far must finish before TMEM/smem go away.
@@ -205,60 +230,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int khalf = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int tile = blockIdx.x; tile < cfg.num_tiles; tile += gridDim.x) {
-            bool ok = true;
-            for (int k = 0; k < cfg.num_kiters; ++k) {
-                float v[32];
-                Prob::fetch_a(p, extra, tile, k, row, khalf * 32, v);
-                int w_ok = 1;
-                if (lane == 0) w_ok = mbar_wait(empty(stage), phase ^ 1u, ctx, kSiteAEmpty);
-                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-                if (!w_ok) { ok = false; break; }
-                const uint32_t a_base = smem_u32(stage_ptr(stage));
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)(khalf * 4 + j));
-                    if constexpr (NP == 2) {
-                        uint32_t h[4], l[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            split_bf16x2(v[8 * j + 2 * e], v[8 * j + 2 * e + 1], h[e], l[e]);
-                        st_shared_v4(a_base + off, h[0], h[1], h[2], h[3]);
-                        st_shared_v4(a_base + kATileBytes + off, l[0], l[1], l[2], l[3]);
-                    } else {
-                        st_shared_v4(a_base + off, pack_bf16x2(v[8 * j], v[8 * j + 1]),
-                                     pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                     pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                                     pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(full_a(stage));
-                if (++stage == S) { stage = 0; phase ^= 1u; }
+        const int k0 = khalf * 32;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        // load cursor runs one stage ahead of the process cursor
+        int ltile = blockIdx.x, lk = 0;
+        int ptile = blockIdx.x, pk = 0;
+        Tile ltl{}, ptl{};
+        if (ltile < cfg.num_tiles) ltl = Prob::tile_info(p, ltile);
+        ptl = ltl;
+        int sa = 0;
+        uint32_t pha = 0;
+        auto advance = [&](int& t, int& kk, Tile& tl) {
+            if (++kk == cfg.num_kiters) {
+                kk = 0;
+                t += gridDim.x;
+                if (t < cfg.num_tiles) tl = Prob::tile_info(p, t);
             }
-            if (!ok) break;
+        };
+        // Returns false when the pipeline is being aborted.
+        auto process = [&](float (&v)[32]) -> bool {
+            Prob::finish_a(p, extra, ptl, pk, row, k0, v);
+            int w_ok = 1;
+            if (lane == 0) w_ok = mbar_wait(a_empty(sa), pha ^ 1u, ctx, kSiteAEmpty);
+            w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+            if (!w_ok) return false;
+            tc_fence_after();
+            split_store_a<NP>(tmem_base + lane_off + kTmemARing + (uint32_t)(sa * 32 * NP) +
+                                  (uint32_t)(k0 / 2),
+                              v);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full(sa));
+            if (++sa == SA) { sa = 0; pha ^= 1u; }
+            advance(ptile, pk, ptl);
+            return true;
+        };
+        float v0[32], v1[32];
+        if (ltile < cfg.num_tiles) {
+            Prob::load_a(p, ltl, lk, row, k0, v0);
+            advance(ltile, lk, ltl);
+        }
+        while (ptile < cfg.num_tiles) {
+            if (ltile < cfg.num_tiles) {
+                Prob::load_a(p, ltl, lk, row, k0, v1);
+                advance(ltile, lk, ltl);
+            }
+            if (!process(v0) || ptile >= cfg.num_tiles) break;
+            if (ltile < cfg.num_tiles) {
+                Prob::load_a(p, ltl, lk, row, k0, v0);
+                advance(ltile, lk, ltl);
+            }
+            if (!process(v1)) break;
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;
         int it = 0;
         for (int tile = blockIdx.x; tile < cfg.num_tiles; tile += gridDim.x, ++it) {
-            const int acc = it & 1;
-            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            const Tile tl = Prob::tile_info(p, tile);
             int w_ok = 1;
-            if (lane == 0) w_ok = mbar_wait(acc_full(acc), acc_phase, ctx, kSiteAccFull);
+            if (lane == 0) w_ok = mbar_wait(acc_full, (uint32_t)it & 1u, ctx, kSiteAccFull);
             w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
             if (!w_ok) break;
             tc_fence_after();
-            const uint32_t taddr =
-                tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-            Prob::epilogue(p, extra, tile, quarter, lane, taddr, BN);
+            Prob::epilogue(p, extra, tl, quarter, lane,
+                           tmem_base + ((uint32_t)(quarter * 32) << 16), BN);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty(acc));
+            if (lane == 0) mbar_arrive(acc_empty);
         }
     }
 
@@ -267,15 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, cfg.tmem_cols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
-}
-
-// Host helpers ------------------------------------------------------------------
-inline uint32_t tmem_cols_for(int BN) {
-    uint32_t c = 32;
-    while (c < (uint32_t)(2 * BN)) c <<= 1;
-    return c;
 }
 
 }  // namespace nrc

@@ -5,7 +5,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/nrc.h"
+#include "nrc.h"
 
 namespace nrc {
 

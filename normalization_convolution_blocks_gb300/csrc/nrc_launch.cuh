@@ -10,31 +10,31 @@
 namespace nrc {
 
 struct GemmPlan {
-    int BN, num_tiles, num_kiters, stages;
-    uint32_t stage_bytes, extra_bytes, smem_bytes;
+    int BN, num_tiles, num_kiters, b_stages;
+    uint32_t b_stage_bytes, extra_bytes, smem_bytes;
 };
 
-// Pipeline depth: as many stages as fit in the opt-in shared memory next to
-// the bookkeeping and the block's extra bytes (at most kMaxStages).
+// B ring depth: as many stages as fit in the opt-in shared memory next to the
+// bookkeeping and the block's extra bytes (at most kMaxStages).
 inline GemmPlan make_gemm_plan(int BN, int num_tiles, int num_kiters, int NP,
                                uint32_t extra_bytes) {
     GemmPlan g{};
     g.BN = BN;
     g.num_tiles = num_tiles;
     g.num_kiters = num_kiters;
-    g.stage_bytes = (uint32_t)NP * (kATileBytes + (uint32_t)BN * 128u);
+    g.b_stage_bytes = (uint32_t)NP * (uint32_t)BN * 128u;
     g.extra_bytes = extra_bytes;
-    const uint32_t fixed = 1024u + gemm_bookkeeping_bytes(kMaxStages) + extra_bytes;
-    g.stages = std::min<int>(kMaxStages, (int)((kMaxSmemBytes - fixed) / g.stage_bytes));
-    g.smem_bytes =
-        1024u + (uint32_t)g.stages * g.stage_bytes + gemm_bookkeeping_bytes(g.stages) + extra_bytes;
+    const uint32_t fixed = 1024u + gemm_bookkeeping_bytes() + extra_bytes;
+    g.b_stages = std::min<int>(kMaxStages, (int)((kMaxSmemBytes - fixed) / g.b_stage_bytes));
+    g.smem_bytes = 1024u + (uint32_t)g.b_stages * g.b_stage_bytes + gemm_bookkeeping_bytes() +
+                   extra_bytes;
     return g;
 }
 
 template <class Prob, int NP>
 inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
                               const GemmPlan& pl, cudaStream_t stream) {
-    if (pl.stages < 2) return NRC_ERR_UNSUPPORTED;
+    if (pl.b_stages < 2) return NRC_ERR_UNSUPPORTED;
     auto kern = gemm_kernel<Prob, NP>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)pl.smem_bytes) != cudaSuccess)
@@ -43,19 +43,13 @@ inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
     cfg.BN = pl.BN;
     cfg.num_tiles = pl.num_tiles;
     cfg.num_kiters = pl.num_kiters;
-    cfg.stages = pl.stages;
-    cfg.stage_bytes = pl.stage_bytes;
-    cfg.tmem_cols = tmem_cols_for(pl.BN);
+    cfg.b_stages = pl.b_stages;
+    cfg.b_stage_bytes = pl.b_stage_bytes;
     cfg.status = device_status_ptr();
     cfg.timeout_ns = wait_timeout_ns();
     if (cfg.status == nullptr) return NRC_ERR_CUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, pl.smem_bytes) !=
-        cudaSuccess)
-        return NRC_ERR_CUDA;
-    // Co-resident CTAs must also fit their TMEM allocations (512 columns per SM).
-    per_sm = std::max(1, std::min(per_sm, (int)(512u / cfg.tmem_cols)));
-    const int grid = std::min(pl.num_tiles, device_sm_count() * per_sm);
+    // Each CTA allocates all 512 TMEM columns, so one CTA per SM.
+    const int grid = std::min(pl.num_tiles, device_sm_count());
     {
         TraceScope ts(name, stream);
         kern<<<grid, kThreads, pl.smem_bytes, stream>>>(p, cfg);
