@@ -96,6 +96,35 @@ nrc_status nrc_prenorm_dilconv_residual(
     void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Allocation-free pre-norm residual block.  The pages have no counterpart:
+ * this is a library convenience, not part of the method.
+ *
+ * Same computation, arguments and errors as nrc_prenorm_dilconv_residual, but
+ * without a workspace: the scratch (the repacked weight image) lives in a
+ * fixed array in the library's own device memory, so the call allocates
+ * nothing.  It is for callers that cannot hand the library scratch memory --
+ * code whose device memory belongs to a host framework's allocator that
+ * forbids side allocations, or loops that must not call cudaMalloc/cudaFree.
+ *
+ * Limit: the array is nrc_prenorm_dilconv_residual_noalloc_max_bytes() (4 MiB),
+ * present on every GPU that loads the library until the process exits; it
+ * holds fp32 C <= 512 or bf16 C <= 768.  Larger C returns NRC_ERR_WORKSPACE.
+ * The first call on a device looks up the array's device address (one
+ * cudaGetSymbolAddress, with that device current); make that first call before
+ * any stream capture.  All calls share the array and each rewrites what it
+ * uses, so nothing needs clearing, but calls that overlap on the GPU (several
+ * streams or host threads at once) race on it.
+ * ------------------------------------------------------------------------ */
+size_t nrc_prenorm_dilconv_residual_noalloc_max_bytes(void);
+
+nrc_status nrc_prenorm_dilconv_residual_noalloc(
+    const void *x, void *out, nrc_dtype dt, int N, int C, int L,
+    int kernel_size, int dilation, int padding,
+    const float *bn_running_mean, const float *bn_running_var,
+    const float *bn_gamma, const float *bn_beta, float bn_eps,
+    const void *conv_weight, const void *conv_bias, void *stream);
+
+/* ------------------------------------------------------------------------
  * Conv1d + GroupNorm ("FW-GLM-5-1 l2_p35", problem analysis and its
  * normalisation kernel)
  *

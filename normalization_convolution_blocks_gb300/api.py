@@ -53,6 +53,9 @@ def load() -> ctypes.CDLL:
         "nrc_prenorm_dilconv_residual_workspace_size": ([i, i], sz),
         "nrc_prenorm_dilconv_residual": ([p, p, i, i, i, i, i, i, i, p, p, p, p, f, p, p, p, sz,
                                           p], i),
+        "nrc_prenorm_dilconv_residual_noalloc_max_bytes": ([], sz),
+        "nrc_prenorm_dilconv_residual_noalloc": ([p, p, i, i, i, i, i, i, i, p, p, p, p, f, p, p,
+                                                  p], i),
         "nrc_conv1d_groupnorm_workspace_size": ([i, i, i, i, i], sz),
         "nrc_conv1d_groupnorm": ([p, p, i, i, i, i, i, i, i, i, p, p, i, p, p, f, p, sz, p], i),
         "nrc_linear_bn_swish_workspace_size": ([i, i, i], sz),
@@ -291,4 +294,28 @@ def trace_records():
         ms = ctypes.c_float()
         _check(lib.nrc_trace_get(i, ctypes.byref(name), ctypes.byref(ms)), "nrc_trace_get")
         out.append((name.value.decode(), float(ms.value)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Allocation-free pre-norm block
+# ---------------------------------------------------------------------------
+def prenorm_dilconv_residual_noalloc(x, bn_running_mean, bn_running_var, bn_gamma, bn_beta,
+                                     bn_eps, conv_weight, conv_bias, dilation, out,
+                                     padding=None, kernel_size=3, stream=None):
+    """The pre-norm block without a workspace, for callers that cannot hand the
+    library scratch memory: its scratch is a fixed 4 MiB array inside the
+    library (fp32 C <= 512, bf16 C <= 768).  All arguments must already be
+    contiguous device tensors of the right dtypes and `out` must be given, so
+    this binding allocates nothing either.  Calls that overlap on the GPU race
+    on the shared scratch."""
+    lib = load()
+    dt = NRC_F32 if x.dtype == torch.float32 else NRC_BF16
+    N, C, L = x.shape
+    padding = dilation if padding is None else padding
+    st = lib.nrc_prenorm_dilconv_residual_noalloc(
+        _ptr(x), _ptr(out), dt, N, C, L, kernel_size, dilation, padding, _ptr(bn_running_mean),
+        _ptr(bn_running_var), _ptr(bn_gamma), _ptr(bn_beta), float(bn_eps), _ptr(conv_weight),
+        _ptr(conv_bias), _stream(stream))
+    _check(st, "nrc_prenorm_dilconv_residual_noalloc")
     return out

@@ -15,6 +15,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "nrc_launch.cuh"
 
@@ -524,4 +525,66 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
             out, p.partials, pl.n_tt * 4, C_out, T, num_groups, gn_gamma, gn_beta, eps);
     }
     return cuda_status(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of nrc_prenorm_dilconv_residual.
+//
+// The regular entry point takes its scratch (the repacked weight image) from a
+// caller-provided workspace.  Some callers cannot provide one: their device
+// memory is owned by a host framework's allocator that forbids side
+// allocations, or they run in a loop where a cudaMalloc/cudaFree (and the
+// device-wide synchronisation it can bring) is not acceptable.  This variant
+// keeps its scratch in a fixed-size array in the library's own device memory
+// instead, so it allocates nothing.
+//
+// The array is kNoAllocScratchBytes (4 MiB) on every GPU that loads the
+// library, held until the process exits; the weight image of fp32 C <= 512
+// (bf16 C <= 768) fits.  Larger C is rejected with NRC_ERR_WORKSPACE.  Every
+// call rewrites the whole image it uses (padding included), so no contents
+// need clearing, but all calls share the one array: calls that overlap on the
+// GPU (two streams, two host threads) race on it.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64];   // device address of g_noalloc_scratch, per device
+
+// Device address of the scratch array on the current device.  The name of a
+// __device__ array in host code is only a host-side stand-in, so the address
+// is looked up (once per device, with that device current).
+nrc_status noalloc_scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NRC_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return NRC_ERR_CUDA;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return NRC_OK;
+}
+}  // namespace
+
+extern "C" size_t nrc_prenorm_dilconv_residual_noalloc_max_bytes(void) {
+    return kNoAllocScratchBytes;
+}
+
+extern "C" nrc_status nrc_prenorm_dilconv_residual_noalloc(
+    const void* x, void* out, nrc_dtype dt, int N, int C, int L, int kernel_size, int dilation,
+    int padding, const float* rm, const float* rv, const float* gamma, const float* beta,
+    float bn_eps, const void* conv_weight, const void* conv_bias, void* stream) {
+    if ((dt != NRC_F32 && dt != NRC_BF16) || C <= 0) return NRC_ERR_INVALID_ARG;
+    if (nrc_prenorm_dilconv_residual_workspace_size(C, dt) > kNoAllocScratchBytes)
+        return NRC_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    const nrc_status s = noalloc_scratch_address(&scratch);
+    if (s != NRC_OK) return s;
+    return nrc_prenorm_dilconv_residual(x, out, dt, N, C, L, kernel_size, dilation, padding, rm,
+                                        rv, gamma, beta, bn_eps, conv_weight, conv_bias, scratch,
+                                        kNoAllocScratchBytes, stream);
 }
