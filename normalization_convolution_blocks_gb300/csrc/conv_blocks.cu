@@ -52,6 +52,7 @@ struct ConvParams {
     const float *rm, *rv, *gamma, *beta;
     float bn_eps;
     const void* bias;       // (Cout) or NULL
+    int bias_off;           // float offset of the staged bias in the extra smem
     const uint8_t* wpack;   // packed weight image
     // group statistics (conv + GroupNorm)
     float4* partials;       // [(n*G + g) * n_tt * 4 + tt*4 + quarter] = (count, mean, M2, 0)
@@ -102,18 +103,24 @@ struct ConvProblem {
     }
 
     static __device__ void setup(const Params& p, uint8_t* extra) {
+        float* ex = reinterpret_cast<float*>(extra);
+        // Conv bias for every (padded) output channel, staged once per CTA so
+        // the epilogue reads it from shared memory.
+        const T* bias = static_cast<const T*>(p.bias);
+        for (int o = threadIdx.x; o < p.n_ot * p.BN; o += blockDim.x)
+            ex[p.bias_off + o] = (bias && o < p.Cout) ? load_f<T>(bias + o) : 0.f;
         if (p.rm == nullptr) return;
         // BN fold: z = max(0, x*scale + shift), scale = gamma/sqrt(rv+eps),
         // shift = beta - rm*scale.  Channels past Cin get 0.
-        float* sc = reinterpret_cast<float*>(extra);
+        float* sc = ex;
         float* sh = sc + p.n_chunks * kBK;
         for (int c = threadIdx.x; c < p.n_chunks * kBK; c += blockDim.x) {
-            float s = 0.f, h = 0.f;
+            float sv = 0.f, h = 0.f;
             if (c < p.Cin) {
-                s = p.gamma[c] / sqrtf(p.rv[c] + p.bn_eps);
-                h = p.beta[c] - p.rm[c] * s;
+                sv = p.gamma[c] / sqrtf(p.rv[c] + p.bn_eps);
+                h = p.beta[c] - p.rm[c] * sv;
             }
-            sc[c] = s;
+            sc[c] = sv;
             sh[c] = h;
         }
     }
@@ -172,44 +179,70 @@ struct ConvProblem {
         return p.wpack + ((size_t)tl.ot * p.n_kiters + kiter) * NP * (size_t)p.BN * 128u;
     }
 
-    static __device__ __forceinline__ void epilogue(const Params& p, const uint8_t*,
+    static __device__ __forceinline__ void epilogue(const Params& p, const uint8_t* extra,
                                                     const Tile& tl, int quarter, int lane,
                                                     uint32_t taddr, int BN) {
         const int t = tl.tt * kBM + quarter * 32 + lane;
         const bool t_ok = t < p.L;
-        const T* bias = static_cast<const T*>(p.bias);
         T* out = static_cast<T*>(p.out);
         const int obase = tl.ot * BN;
         const size_t row0 = (size_t)tl.n * p.Cout;
+        const float* bias_s = reinterpret_cast<const float*>(extra) + p.bias_off + obase;
         if constexpr (EPI == ConvEpi::kResidual) {
-            const T* x = static_cast<const T*>(p.x);
-            // residual of the next 16 channels is loaded one chunk ahead
-            float r[16], rn[16];
+            // out = acc + bias + x.  The residual of a 16-channel chunk is loaded
+            // three chunks ahead so the loads' latency overlaps the drain.  The
+            // tests that select a path are uniform per chunk (and t_ok per
+            // lane), so the drain of a full chunk is straight-line code.
+            const T* xr = static_cast<const T*>(p.x) + (row0 + obase) * p.L + t;
+            T* outr = out + (row0 + obase) * p.L + t;
+            const int ovalid = p.Cout - obase;     // channels of this tile that exist
+            auto fetch = [&](int cc, float (&r)[16]) {
+                if (cc >= BN) return;
+                const T* xp = xr + (size_t)cc * p.L;
+                if (cc + 16 <= ovalid) {
+                    if (t_ok) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int o = obase + i;
-                rn[i] = (t_ok && o < p.Cout) ? load_f<T>(x + (row0 + o) * p.L + t) : 0.f;
-            }
-            for (int cc = 0; cc < BN; cc += 16) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) r[i] = rn[i];
-                if (cc + 16 < BN) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int o = obase + cc + 16 + i;
-                        rn[i] = (t_ok && o < p.Cout) ? load_f<T>(x + (row0 + o) * p.L + t) : 0.f;
+                        for (int i = 0; i < 16; ++i) r[i] = load_f<T>(xp + (size_t)i * p.L);
                     }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        r[i] = (t_ok && cc + i < ovalid) ? load_f<T>(xp + (size_t)i * p.L) : 0.f;
                 }
+            };
+            auto emit = [&](int cc, float (&r)[16]) {
                 float v[16];
                 tmem_ld16(taddr + (uint32_t)cc, v);
+                const float4* b4 = reinterpret_cast<const float4*>(bias_s + cc);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int o = obase + cc + i;
-                    if (t_ok && o < p.Cout) {
-                        const float b = bias ? load_f<T>(bias + o) : 0.f;
-                        store_f<T>(out + (row0 + o) * p.L + t, v[i] + b + r[i]);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    const float4 bq = b4[q];
+                    v[4 * q] += bq.x + r[4 * q];
+                    v[4 * q + 1] += bq.y + r[4 * q + 1];
+                    v[4 * q + 2] += bq.z + r[4 * q + 2];
+                    v[4 * q + 3] += bq.w + r[4 * q + 3];
                 }
+                T* op = outr + (size_t)cc * p.L;
+                if (cc + 16 <= ovalid) {
+                    if (t_ok) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) store_f<T>(op + (size_t)i * p.L, v[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (t_ok && cc + i < ovalid) store_f<T>(op + (size_t)i * p.L, v[i]);
+                }
+                fetch(cc + 48, r);              // refill this buffer three chunks ahead
+            };
+            float r0[16], r1[16], r2[16];
+            fetch(0, r0);
+            fetch(16, r1);
+            fetch(32, r2);
+            for (int cc = 0; cc < BN; cc += 48) {
+                emit(cc, r0);
+                if (cc + 16 < BN) emit(cc + 16, r1);
+                if (cc + 32 < BN) emit(cc + 32, r2);
             }
         } else {
             // y -> out, and per-(n, group, t tile, warp) statistics of y.
@@ -221,7 +254,7 @@ struct ConvProblem {
                 for (int i = 0; i < 16; ++i) {
                     const int o = obase + cc + i;
                     if (o >= p.Cout) break;                 // uniform across the warp
-                    const float y = v[i] + (bias ? load_f<T>(bias + o) : 0.f);
+                    const float y = v[i] + bias_s[cc + i];
                     if (t_ok) {
                         store_f<T>(out + (row0 + o) * p.L + t, y);
                         cnt += 1.f;                          // Welford update
@@ -370,7 +403,8 @@ static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn)
     pl.n_chunks = ceil_div(Cin, kBK);
     pl.n_tt = ceil_div(L, kBM);
     const long long tiles = (long long)N * pl.n_tt * pl.n_ot;
-    const uint32_t extra = with_bn ? (uint32_t)(2 * pl.n_chunks * kBK * 4) : 0u;
+    const uint32_t extra = (with_bn ? (uint32_t)(2 * pl.n_chunks * kBK * 4) : 0u) +
+                           (uint32_t)(pl.n_ot * BN * 4);
     pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), 3 * pl.n_chunks, NP,
                           extra);
     pl.wpack_bytes = (size_t)pl.n_ot * pl.g.num_kiters * NP * BN * 128;
@@ -428,6 +462,7 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual(
     p.beta = beta;
     p.bn_eps = bn_eps;
     p.bias = conv_bias;
+    p.bias_off = 2 * pl.n_chunks * kBK;
     p.wpack = static_cast<const uint8_t*>(workspace);
     const size_t units = pl.wpack_bytes / 16 / NP;
     if (dt == NRC_F32) {
@@ -505,6 +540,7 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     p.n_kiters = pl.g.num_kiters;
     p.BN = pl.g.BN;
     p.bias = conv_bias;
+    p.bias_off = 0;
     p.wpack = ws;
     p.partials = reinterpret_cast<float4*>(ws + gn_partials_offset(pl));
     p.G = num_groups;
