@@ -107,7 +107,8 @@ struct ConvProblem {
         // Conv bias for every (padded) output channel, staged once per CTA so
         // the epilogue reads it from shared memory.
         const T* bias = static_cast<const T*>(p.bias);
-        for (int o = threadIdx.x; o < p.n_ot * p.BN; o += blockDim.x)
+        // (32 zero floats past the last tile, so vector reads never leave the region)
+        for (int o = threadIdx.x; o < p.n_ot * p.BN + 32; o += blockDim.x)
             ex[p.bias_off + o] = (bias && o < p.Cout) ? load_f<T>(bias + o) : 0.f;
         if (p.rm == nullptr) return;
         // BN fold: z = max(0, x*scale + shift), scale = gamma/sqrt(rv+eps),
@@ -245,27 +246,69 @@ struct ConvProblem {
                 if (cc + 32 < BN) emit(cc + 32, r2);
             }
         } else {
-            // y -> out, and per-(n, group, t tile, warp) statistics of y.
+            // y -> out, and per-(n, group, t tile, warp) statistics of y.  A
+            // group's channels are contiguous.  Each run of a group inside a
+            // 16-channel chunk is reduced two-pass in registers (count, mean,
+            // M2), folded into the group's running triple with Chan's update,
+            // and merged across the warp when the group ends.  Every test below
+            // is uniform across the warp except t_ok (invalid rows count 0).
+            const int ovalid = p.Cout - obase;
             float cnt = 0.f, mean = 0.f, m2 = 0.f;
-            for (int cc = 0; cc < BN; cc += 16) {
+            const float tw = t_ok ? 1.f : 0.f;
+            for (int cc = 0; cc < BN && cc < ovalid; cc += 16) {
                 float v[16];
                 tmem_ld16(taddr + (uint32_t)cc, v);
+                const float4* b4 = reinterpret_cast<const float4*>(bias_s + cc);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int o = obase + cc + i;
-                    if (o >= p.Cout) break;                 // uniform across the warp
-                    const float y = v[i] + bias_s[cc + i];
+                for (int q = 0; q < 4; ++q) {
+                    const float4 bq = b4[q];
+                    v[4 * q] += bq.x;
+                    v[4 * q + 1] += bq.y;
+                    v[4 * q + 2] += bq.z;
+                    v[4 * q + 3] += bq.w;
+                }
+                T* op = out + (row0 + obase + cc) * p.L + t;
+                const int n = min(16, ovalid - cc);
+                if (n == 16) {
                     if (t_ok) {
-                        store_f<T>(out + (row0 + o) * p.L + t, y);
-                        cnt += 1.f;                          // Welford update
-                        const float d = y - mean;
-                        mean += d / cnt;
-                        m2 += d * (y - mean);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) store_f<T>(op + (size_t)i * p.L, v[i]);
                     }
-                    if ((o + 1) % p.cpg == 0) {              // last channel of group
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (t_ok && i < n) store_f<T>(op + (size_t)i * p.L, v[i]);
+                }
+                // runs [i0, i1) of one group inside this chunk
+                int i0 = 0;
+                while (i0 < n) {
+                    const int o0 = obase + cc + i0;
+                    const int gend = (o0 / p.cpg + 1) * p.cpg;        // first channel of next group
+                    const int i1 = min(n, gend - (obase + cc));
+                    float s = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) s += (i >= i0 && i < i1) ? v[i] : 0.f;
+                    const float k = (float)(i1 - i0);
+                    const float sm = s / k;
+                    float sq = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float d = (i >= i0 && i < i1) ? v[i] - sm : 0.f;
+                        sq = fmaf(d, d, sq);
+                    }
+                    const float kb = k * tw;                           // this run's count
+                    const float nab = cnt + kb;
+                    if (nab > 0.f) {
+                        const float delta = sm - mean;
+                        const float fb = kb / nab;
+                        mean += delta * fb;
+                        m2 += sq * tw + delta * delta * cnt * fb;
+                        cnt = nab;
+                    }
+                    if (obase + cc + i1 == gend) {                     // group complete
                         warp_merge_stats(cnt, mean, m2);
                         if (lane == 0) {
-                            const int g = o / p.cpg;
+                            const int g = o0 / p.cpg;
                             p.partials[((size_t)(tl.n * p.G + g) * p.n_tt + tl.tt) * 4 + quarter] =
                                 make_float4(cnt, mean, m2, 0.f);
                         }
@@ -273,6 +316,7 @@ struct ConvProblem {
                         mean = 0.f;
                         m2 = 0.f;
                     }
+                    i0 = i1;
                 }
             }
         }
@@ -404,7 +448,7 @@ static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn)
     pl.n_tt = ceil_div(L, kBM);
     const long long tiles = (long long)N * pl.n_tt * pl.n_ot;
     const uint32_t extra = (with_bn ? (uint32_t)(2 * pl.n_chunks * kBK * 4) : 0u) +
-                           (uint32_t)(pl.n_ot * BN * 4);
+                           (uint32_t)((pl.n_ot * BN + 32) * 4);
     pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), 3 * pl.n_chunks, NP,
                           extra);
     pl.wpack_bytes = (size_t)pl.n_ot * pl.g.num_kiters * NP * BN * 128;

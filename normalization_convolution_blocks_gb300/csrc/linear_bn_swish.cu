@@ -89,20 +89,33 @@ struct LinearProblem {
         const bool j_ok = j < p.OUT;
         const float lb = (j_ok && p.lin_bias) ? __ldg(p.lin_bias + j) : 0.f;
         const int b0 = tl.bt * BN;
+        const int bvalid = p.B - b0;               // batch rows of this tile that exist
         float cnt = 0.f, mean = 0.f, m2 = 0.f;
-        for (int cc = 0; cc < BN; cc += 16) {
+        float* outj = p.out + (size_t)b0 * p.OUT + j;
+        for (int cc = 0; cc < BN && cc < bvalid; cc += 16) {
             float v[16];
             tmem_ld16(taddr + (uint32_t)cc, v);
+            const int n = min(16, bvalid - cc);   // uniform
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] += lb;
+            float* op = outj + (size_t)cc * p.OUT;
+            if (j_ok) {
+                if (n == 16) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) op[(size_t)i * p.OUT] = v[i];
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (i < n) op[(size_t)i * p.OUT] = v[i];
+                }
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const int b = b0 + cc + i;
-                if (j_ok && b < p.B) {
-                    const float y = v[i] + lb;
-                    p.out[(size_t)b * p.OUT + j] = y;
-                    cnt += 1.f;                       // Welford over the tile's rows
-                    const float d = y - mean;
+                if (i < n) {                         // Welford over the tile's rows
+                    cnt += 1.f;
+                    const float d = v[i] - mean;
                     mean += d / cnt;
-                    m2 += d * (y - mean);
+                    m2 += d * (v[i] - mean);
                 }
             }
         }

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "nrc_gemm.cuh"
 #include "nrc_host.h"
@@ -36,9 +37,18 @@ inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
                               const GemmPlan& pl, cudaStream_t stream) {
     if (pl.b_stages < 2) return NRC_ERR_UNSUPPORTED;
     auto kern = gemm_kernel<Prob, NP>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)pl.smem_bytes) != cudaSuccess)
-        return NRC_ERR_CUDA;
+    // The opt-in shared-memory size is raised once per device and kernel
+    // (to the maximum), so calls issue no host API work between launches.
+    static std::atomic<unsigned long long> smem_set_mask{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NRC_ERR_CUDA;
+    if (!(smem_set_mask.load() & (1ull << dev))) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxSmemBytes) != cudaSuccess)
+            return NRC_ERR_CUDA;
+        smem_set_mask.fetch_or(1ull << dev);
+    }
+    if (pl.smem_bytes > (uint32_t)kMaxSmemBytes) return NRC_ERR_UNSUPPORTED;
     GemmCfg cfg{};
     cfg.BN = pl.BN;
     cfg.num_tiles = pl.num_tiles;
