@@ -46,7 +46,12 @@ L2_FLUSH_BYTES = 256 << 20
 # DRAM traffic (read + write bytes) of one launch of the dominant kernel, from
 # one ncu capture (profiles/), keyed by workload; valid only while the kernel
 # sources hash to the recorded value.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "prenorm_block_f32": {"bytes": 222758656, "src_hash": "d0d069f37ab65ead",
+                          "profile": "profiles/gemm_prenorm_block_f32_N32_C256_L4096_d128.md"},
+    "linear_bn_swish_f32": {"bytes": 359000064, "src_hash": "d0d069f37ab65ead",
+                            "profile": "profiles/gemm_linear_bn_swish_f32_B1024_IN8192_OUT8192.md"},
+}
 
 
 def kernel_source_hash() -> str:
