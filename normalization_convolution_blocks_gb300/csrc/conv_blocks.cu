@@ -180,9 +180,10 @@ struct ConvProblem {
         return p.wpack + ((size_t)tl.ot * p.n_kiters + kiter) * NP * (size_t)p.BN * 128u;
     }
 
-    static __device__ __forceinline__ void epilogue(const Params& p, const uint8_t* extra,
+    template <class Acquire>
+    static __device__ __forceinline__ bool epilogue(const Params& p, const uint8_t* extra,
                                                     const Tile& tl, int quarter, int lane,
-                                                    uint32_t taddr, int BN) {
+                                                    uint32_t taddr, int BN, Acquire& acquire) {
         const int t = tl.tt * kBM + quarter * 32 + lane;
         const bool t_ok = t < p.L;
         T* out = static_cast<T*>(p.out);
@@ -190,10 +191,11 @@ struct ConvProblem {
         const size_t row0 = (size_t)tl.n * p.Cout;
         const float* bias_s = reinterpret_cast<const float*>(extra) + p.bias_off + obase;
         if constexpr (EPI == ConvEpi::kResidual) {
-            // out = acc + bias + x.  The residual of a 16-channel chunk is loaded
-            // three chunks ahead so the loads' latency overlaps the drain.  The
-            // tests that select a path are uniform per chunk (and t_ok per
-            // lane), so the drain of a full chunk is straight-line code.
+            // out = acc + bias + x.  The residual of the first four 16-channel
+            // chunks is loaded before the accumulator is ready (this warp is
+            // otherwise idle during the mainloop), later chunks four ahead of
+            // the drain.  Path tests are uniform per chunk (t_ok per lane), so
+            // a full chunk drains as straight-line code.
             const T* xr = static_cast<const T*>(p.x) + (row0 + obase) * p.L + t;
             T* outr = out + (row0 + obase) * p.L + t;
             const int ovalid = p.Cout - obase;     // channels of this tile that exist
@@ -234,16 +236,19 @@ struct ConvProblem {
                     for (int i = 0; i < 16; ++i)
                         if (t_ok && cc + i < ovalid) store_f<T>(op + (size_t)i * p.L, v[i]);
                 }
-                fetch(cc + 48, r);              // refill this buffer three chunks ahead
+                fetch(cc + 64, r);              // refill this buffer four chunks ahead
             };
-            float r0[16], r1[16], r2[16];
+            float r0[16], r1[16], r2[16], r3[16];
             fetch(0, r0);
             fetch(16, r1);
             fetch(32, r2);
-            for (int cc = 0; cc < BN; cc += 48) {
+            fetch(48, r3);
+            if (!acquire()) return false;
+            for (int cc = 0; cc < BN; cc += 64) {
                 emit(cc, r0);
                 if (cc + 16 < BN) emit(cc + 16, r1);
                 if (cc + 32 < BN) emit(cc + 32, r2);
+                if (cc + 48 < BN) emit(cc + 48, r3);
             }
         } else {
             // y -> out, and per-(n, group, t tile, warp) statistics of y.  A
@@ -252,6 +257,7 @@ struct ConvProblem {
             // M2), folded into the group's running triple with Chan's update,
             // and merged across the warp when the group ends.  Every test below
             // is uniform across the warp except t_ok (invalid rows count 0).
+            if (!acquire()) return false;
             const int ovalid = p.Cout - obase;
             float cnt = 0.f, mean = 0.f, m2 = 0.f;
             const float tw = t_ok ? 1.f : 0.f;
@@ -320,6 +326,7 @@ struct ConvProblem {
                 }
             }
         }
+        return true;
     }
 };
 

@@ -82,9 +82,11 @@ struct LinearProblem {
         return p.xpack + ((size_t)tl.bt * p.n_kiters + kiter) * 2 * (size_t)p.BN * 128u;
     }
 
-    static __device__ __forceinline__ void epilogue(const Params& p, const uint8_t*,
+    template <class Acquire>
+    static __device__ __forceinline__ bool epilogue(const Params& p, const uint8_t*,
                                                     const Tile& tl, int quarter, int lane,
-                                                    uint32_t taddr, int BN) {
+                                                    uint32_t taddr, int BN, Acquire& acquire) {
+        if (!acquire()) return false;
         const int j = tl.jt * kBM + quarter * 32 + lane;
         const bool j_ok = j < p.OUT;
         const float lb = (j_ok && p.lin_bias) ? __ldg(p.lin_bias + j) : 0.f;
@@ -120,6 +122,7 @@ struct LinearProblem {
             }
         }
         if (j_ok) p.partials[(size_t)tl.bt * p.OUT + j] = make_float4(cnt, mean, m2, 0.f);
+        return true;
     }
 };
 

@@ -89,10 +89,14 @@ __device__ __forceinline__ void split_store_a(uint32_t taddr_hi, const float (&v
 //        -> the block's transform, in place (runs after the loads have landed)
 //   static __device__ const void* b_src(const Params&, const Tile&, int kiter)
 //        -> packed B image of the stage: NP parts of BN rows x 128 B, swizzled
-//   static __device__ void epilogue(const Params&, const uint8_t* extra, const Tile&,
-//                                   int quarter, int lane, uint32_t taddr, int BN)
-//        -> drains TMEM columns [taddr, taddr + BN) of its lane quarter (every lane
-//           executes the tcgen05.ld calls)
+//   template <class Acquire>
+//   static __device__ bool epilogue(const Params&, const uint8_t* extra, const Tile&,
+//                                   int quarter, int lane, uint32_t taddr, int BN,
+//                                   Acquire& acquire)
+//        -> may issue loads that do not need the accumulator, then calls acquire()
+//           (waits for the tile's accumulator; false = pipeline aborted, return
+//           false), then drains TMEM columns [taddr, taddr + BN) of its lane
+//           quarter (every lane executes the tcgen05.ld calls)
 template <class Prob, int NP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const typename Prob::Params p, const GemmCfg cfg) {
@@ -288,13 +292,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         for (int tile = blockIdx.x; tile < cfg.num_tiles; tile += gridDim.x, ++it) {
             const Tile tl = Prob::tile_info(p, tile);
-            int w_ok = 1;
-            if (lane == 0) w_ok = mbar_wait(acc_full, (uint32_t)it & 1u, ctx, kSiteAccFull);
-            w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-            if (!w_ok) break;
-            tc_fence_after();
-            Prob::epilogue(p, extra, tl, quarter, lane,
-                           tmem_base + ((uint32_t)(quarter * 32) << 16), BN);
+            // The block's epilogue calls acquire() once it has issued whatever
+            // it can load before the accumulator is ready.
+            auto acquire = [&]() -> bool {
+                int w_ok = 1;
+                if (lane == 0) w_ok = mbar_wait(acc_full, (uint32_t)it & 1u, ctx, kSiteAccFull);
+                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+                if (w_ok) tc_fence_after();
+                return w_ok != 0;
+            };
+            if (!Prob::epilogue(p, extra, tl, quarter, lane,
+                                tmem_base + ((uint32_t)(quarter * 32) << 16), BN, acquire))
+                break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
