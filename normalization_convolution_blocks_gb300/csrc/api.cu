@@ -56,6 +56,41 @@ int device_sm_count() {
 }
 
 namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+}  // namespace
+
+bool encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                          const uint64_t dims[3], const uint64_t strides[2],
+                          const uint32_t box[3], bool nan_fill) {
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t gdim[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t gstride[2] = {strides[0], strides[1]};
+    const cuuint32_t bdim[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return fn(map, dtype, 3, const_cast<void*>(base), gdim, gstride, bdim, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              nan_fill ? CU_TENSOR_MAP_FLOAT_OOB_FILL_NAN_REQUEST_ZERO_FMA
+                       : CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 struct TraceRec {
     const char* name;
     cudaEvent_t start, stop;

@@ -6,10 +6,14 @@
 // GEMM view of one sample n: D[t][o] = sum_tap sum_c z[c][t - pad + tap*dil] * W[o][c][tap].
 // Tile rows are 128 consecutive t, tile columns BN output channels; the K loop
 // runs over (tap, 64-channel chunk).  The A operand (activations) is produced
-// in shared memory by the prologue warps: the conv input for the tile's shifted
+// in tensor memory by the prologue warps: the conv input for the tile's shifted
 // window, with BN+ReLU applied (block) and the zero padding applied after it,
-// split into bf16 hi/lo parts for fp32 storage.  The B operand (weights) is
-// repacked once per call into the exact shared-memory image the MMA reads.
+// split into bf16 hi/lo parts for fp32 storage.  When the rows of x are 16-byte
+// aligned, each prologue warp gathers its part of a tap's shifted window as a
+// TMA box (32 channels x 32 rows, start rounded down to 16 bytes) with
+// out-of-range rows filled by the copy itself; otherwise it loads x directly.
+// The B operand (weights) is repacked once per call into the exact
+// shared-memory image the MMA reads.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -43,6 +47,7 @@ __device__ __forceinline__ void store_f<__nv_bfloat16>(__nv_bfloat16* p, float v
 enum class ConvEpi { kResidual, kGroupStats };
 
 struct ConvParams {
+    CUtensorMap xmap;       // x as (L, Cin, N) boxes of (32 + 16/esize) x 32 x 1 (staged A)
     const void* x;          // (N, Cin, L)
     void* out;              // (N, Cout, L)
     int N, Cin, Cout, L;
@@ -93,10 +98,14 @@ __device__ __forceinline__ void warp_merge_stats(float& cnt, float& mean, float&
     }
 }
 
-template <typename T, ConvEpi EPI>
+template <typename T, ConvEpi EPI, bool STAGED>
 struct ConvProblem {
     using Params = ConvParams;
     using Tile = ConvTile;
+    static constexpr bool kStagedA = STAGED;
+    static constexpr int kAlign = 16 / (int)sizeof(T);   // box starts on 16-byte boundaries
+    static constexpr int kBoxW = 32 + kAlign;             // rows (time positions) per box
+    static constexpr uint32_t kBoxBytes = (uint32_t)(kBoxW * 32 * sizeof(T));
 
     static __device__ __forceinline__ Tile tile_info(const Params& p, int tile) {
         return conv_tile(p, tile);
@@ -152,6 +161,55 @@ struct ConvProblem {
         } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;   // zero padding of the conv input
+        }
+    }
+
+    // Staged A.  The warp's rows t0 + 32*quarter .. +32 read input rows from
+    // s = t0 + 32*quarter - pad + tap*dil; the box starts at s rounded down to
+    // the 16-byte boundary and the warp reads from offset s mod kAlign.  Rows
+    // outside [0, L) and channels past Cin come back as the map's fill: NaN
+    // when BN precedes the conv (max(NaN*scale + shift, 0) = 0, so the padding
+    // is applied after BN+ReLU, as the block defines it), zero otherwise.
+    static __device__ __forceinline__ int box_row0(const Params& p, const Tile& tl, int tap,
+                                                   int quarter) {
+        return tl.tt * kBM + quarter * 32 - p.pad + tap * p.dil;
+    }
+
+    static __device__ __forceinline__ void issue_a_box(const Params& p, const Tile& tl,
+                                                       int kiter, int quarter, int khalf,
+                                                       uint32_t dst, uint32_t bar) {
+        const int tap = kiter >= 2 * p.n_chunks ? 2 : (kiter >= p.n_chunks ? 1 : 0);
+        const int chunk = kiter - tap * p.n_chunks;
+        const int s = box_row0(p, tl, tap, quarter);
+        tma_load_3d(dst, &p.xmap, s & ~(kAlign - 1), chunk * kBK + khalf * 32, tl.n, bar);
+    }
+
+    static __device__ __forceinline__ void read_a(const Params& p, const uint8_t* extra,
+                                                  const Tile& tl, int kiter, int row, int k0,
+                                                  int lane, uint32_t box, float (&v)[32]) {
+        const int tap = kiter >= 2 * p.n_chunks ? 2 : (kiter >= p.n_chunks ? 1 : 0);
+        const int chunk = kiter - tap * p.n_chunks;
+        const int rem = box_row0(p, tl, tap, row >> 5) & (kAlign - 1);
+        const uint32_t a = box + (uint32_t)((lane + rem) * (int)sizeof(T));
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t ai = a + (uint32_t)(i * kBoxW * (int)sizeof(T));
+            if constexpr (sizeof(T) == 4)
+                v[i] = ld_shared_f32(ai);
+            else
+                v[i] = ld_shared_bf16(ai);
+        }
+        if (p.rm == nullptr) return;                   // zero fill is the padding
+        const int c0 = chunk * kBK + k0;
+        const float4* sc = reinterpret_cast<const float4*>(extra) + c0 / 4;
+        const float4* sh = reinterpret_cast<const float4*>(extra) + (p.n_chunks * kBK + c0) / 4;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 a4 = sc[q], b4 = sh[q];
+            v[4 * q] = fmaxf(fmaf(v[4 * q], a4.x, b4.x), 0.f);
+            v[4 * q + 1] = fmaxf(fmaf(v[4 * q + 1], a4.y, b4.y), 0.f);
+            v[4 * q + 2] = fmaxf(fmaf(v[4 * q + 2], a4.z, b4.z), 0.f);
+            v[4 * q + 3] = fmaxf(fmaf(v[4 * q + 3], a4.w, b4.w), 0.f);
         }
     }
 
@@ -447,7 +505,8 @@ struct ConvPlan {
     size_t wpack_bytes;
 };
 
-static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn) {
+static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn,
+                          uint32_t x_box_bytes = 0) {
     ConvPlan pl{};
     const int BN = Cout <= 256 ? ((Cout + 15) / 16) * 16 : 256;
     pl.n_ot = ceil_div(Cout, BN);
@@ -457,9 +516,39 @@ static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn)
     const uint32_t extra = (with_bn ? (uint32_t)(2 * pl.n_chunks * kBK * 4) : 0u) +
                            (uint32_t)((pl.n_ot * BN + 32) * 4);
     pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), 3 * pl.n_chunks, NP,
-                          extra);
+                          extra, x_box_bytes);
     pl.wpack_bytes = (size_t)pl.n_ot * pl.g.num_kiters * NP * BN * 128;
     return pl;
+}
+
+// Tensor map of x for the staged A path: (L, Cin, N) with boxes of
+// (32 + 16/esize) rows x 32 channels x 1 sample.  Needs 16-byte aligned rows;
+// false (use the register path) when they are not or the driver refuses.
+template <typename T>
+static bool make_x_map(ConvParams& p, const void* x, int N, int Cin, int L, bool nan_fill) {
+    constexpr size_t es = sizeof(T);
+    if (!aligned(x, 16) || ((size_t)L * es) % 16 != 0) return false;
+    const uint64_t dims[3] = {(uint64_t)L, (uint64_t)Cin, (uint64_t)N};
+    const uint64_t strides[2] = {(uint64_t)L * es, (uint64_t)Cin * L * es};
+    const uint32_t box[3] = {(uint32_t)(32 + 16 / es), 32u, 1u};
+    return encode_tensor_map_3d(
+        &p.xmap, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x,
+        dims, strides, box, nan_fill);
+}
+
+// Plans the conv GEMM, staged when x allows it and the slots fit; fills the
+// map and returns whether the staged kernel runs.
+template <typename T>
+static bool plan_conv_staged(ConvParams& p, ConvPlan& pl, int N, int Cin, int Cout, int L,
+                             bool with_bn) {
+    constexpr int NP = sizeof(T) == 4 ? 2 : 1;
+    constexpr uint32_t box_bytes = (uint32_t)((32 + 16 / sizeof(T)) * 32 * sizeof(T));
+    if (make_x_map<T>(p, p.x, N, Cin, L, with_bn)) {
+        pl = plan_conv(N, Cin, Cout, L, NP, with_bn, box_bytes);
+        if (pl.g.b_stages >= 2 && pl.g.x_depth >= 2) return true;
+    }
+    pl = plan_conv(N, Cin, Cout, L, NP, with_bn);
+    return false;
 }
 
 }  // namespace nrc
@@ -488,13 +577,15 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual(
     if (ranges_overlap(x, bytes, out, bytes)) return NRC_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return NRC_ERR_ALIGNMENT;
     const int NP = dt == NRC_F32 ? 2 : 1;
-    const ConvPlan pl = plan_conv(N, C, C, L, NP, true);
+    ConvPlan pl = plan_conv(N, C, C, L, NP, true);
     if (workspace_bytes < pl.wpack_bytes) return NRC_ERR_WORKSPACE;
     if ((long long)N * pl.n_tt * pl.n_ot >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     ConvParams p{};
     p.x = x;
+    const bool staged = dt == NRC_F32 ? plan_conv_staged<float>(p, pl, N, C, C, L, true)
+                                      : plan_conv_staged<__nv_bfloat16>(p, pl, N, C, C, L, true);
     p.out = out;
     p.N = N;
     p.Cin = C;
@@ -524,8 +615,11 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual(
                 pl.g.BN, pl.n_ot, pl.n_chunks);
         }
         if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
-        return launch_gemm<ConvProblem<float, ConvEpi::kResidual>, 2>("prenorm_block_gemm", p,
-                                                                      pl.g, st);
+        if (staged)
+            return launch_gemm<ConvProblem<float, ConvEpi::kResidual, true>, 2>(
+                "prenorm_block_gemm", p, pl.g, st);
+        return launch_gemm<ConvProblem<float, ConvEpi::kResidual, false>, 2>(
+            "prenorm_block_gemm", p, pl.g, st);
     }
     {
         TraceScope ts("pack_conv_weight", st);
@@ -534,8 +628,11 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual(
             C, pl.g.BN, pl.n_ot, pl.n_chunks);
     }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
-    return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual>, 1>("prenorm_block_gemm",
-                                                                          p, pl.g, st);
+    if (staged)
+        return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual, true>, 1>(
+            "prenorm_block_gemm", p, pl.g, st);
+    return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual, false>, 1>(
+        "prenorm_block_gemm", p, pl.g, st);
 }
 
 static size_t gn_partials_offset(const ConvPlan& pl) {
@@ -569,7 +666,7 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     if (ranges_overlap(x, (size_t)N * C_in * T * 4, out, (size_t)N * C_out * T * 4))
         return NRC_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return NRC_ERR_ALIGNMENT;
-    const ConvPlan pl = plan_conv(N, C_in, C_out, T, 2, false);
+    ConvPlan pl = plan_conv(N, C_in, C_out, T, 2, false);
     if (workspace_bytes < nrc_conv1d_groupnorm_workspace_size(N, C_in, C_out, T, num_groups))
         return NRC_ERR_WORKSPACE;
     if ((long long)N * pl.n_tt * pl.n_ot >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
@@ -578,6 +675,7 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     ConvParams p{};
     p.x = x;
+    const bool staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
     p.out = out;
     p.N = N;
     p.Cin = C_in;
@@ -604,7 +702,10 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
     nrc_status s =
-        launch_gemm<ConvProblem<float, ConvEpi::kGroupStats>, 2>("conv_gn_gemm", p, pl.g, st);
+        staged ? launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true>, 2>("conv_gn_gemm",
+                                                                               p, pl.g, st)
+               : launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, false>, 2>(
+                     "conv_gn_gemm", p, pl.g, st);
     if (s != NRC_OK) return s;
     {
         TraceScope ts("groupnorm_finalize_normalize", st);

@@ -39,6 +39,7 @@ struct LinearTile {
 struct LinearProblem {
     using Params = LinearParams;
     using Tile = LinearTile;
+    static constexpr bool kStagedA = false;
 
     // Tiles of one feature block are adjacent, so the CTAs reading the same
     // weight rows run together and the weight is fetched from HBM once.

@@ -4,7 +4,11 @@
 //
 //   * A (the activation side) is produced by eight prologue warps: each block's
 //     own load-and-transform, split into bf16 parts and written straight into
-//     tensor memory with tcgen05.st; the MMA reads A from TMEM.
+//     tensor memory with tcgen05.st; the MMA reads A from TMEM.  With a staged
+//     A source (Prob::kStagedA) every prologue warp first pulls its raw input
+//     box into a small private ring of shared-memory slots with tiled TMA
+//     copies (cp.async.bulk.tensor), D stages ahead, and transforms from there;
+//     otherwise it loads the raw values into registers one stage ahead.
 //   * B (the weight side) is bulk-copied (cp.async.bulk) from a pre-packed
 //     global image into a ring of shared-memory stages in the 128-byte swizzle
 //     layout the MMA's shared-memory descriptor expects.
@@ -23,6 +27,9 @@
 //   warps 2-9   A producers: warp w owns TMEM lanes 32*(w%4).. (tile rows), K half (w-2)/4
 //   warps 10-13 epilogue: warp w drains TMEM lanes 32*(w%4)..
 //
+// Shared memory: [B ring][A-source slots: 8 warps x D][barriers, TMEM slot,
+// abort flag][the block's extra bytes].
+//
 // TMEM columns: [0, BN) accumulator; [256, 512) A ring, stage s at
 // 256 + s*32*NP (hi part: 32 columns = 64 bf16 of K; then the lo part).
 #pragma once
@@ -37,13 +44,16 @@ constexpr int kBM = 128;            // rows of a tile (MMA M)
 constexpr int kBK = 64;             // K elements per stage (one 128-byte swizzle row)
 constexpr int kUMMA_K = 16;         // K of one bf16 MMA
 constexpr int kMaxStages = 8;
+constexpr int kProducerWarps = 8;
+constexpr int kMaxXDepth = 4;       // A-source slots per producer warp (staged A)
+constexpr int kNumBars = 4 * kMaxStages + 5 + kProducerWarps * kMaxXDepth;
 constexpr int kMaxSmemBytes = 232448;          // 227 KB opt-in per CTA
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemARing = 256;           // first column of the A ring
 
 enum WaitSite : int {
     kSiteBEmpty = 1, kSiteAEmpty = 2, kSiteAccEmpty = 3, kSiteFullA = 4, kSiteFullB = 5,
-    kSiteAccFull = 6
+    kSiteAccFull = 6, kSiteFullX = 7
 };
 
 struct GemmCfg {
@@ -52,13 +62,16 @@ struct GemmCfg {
     int num_kiters;         // K stages per tile
     int b_stages;           // depth of the shared-memory B ring
     uint32_t b_stage_bytes; // NP * BN * 128
+    int x_depth;            // A-source slots per producer warp (0: A loaded to registers)
+    uint32_t x_box_bytes;   // bytes of one slot (a multiple of 128)
     int* status;            // device status word
     unsigned long long timeout_ns;
 };
 
-// Shared-memory bookkeeping after the B stages: barriers and two words.
+// Shared-memory bookkeeping after the B stages and A-source slots: barriers
+// and two words.
 __host__ __device__ constexpr uint32_t gemm_bookkeeping_bytes() {
-    return (((uint32_t)(4 * kMaxStages + 5) * 8u + 16u) + 63u) & ~63u;
+    return (((uint32_t)kNumBars * 8u + 16u) + 63u) & ~63u;
 }
 
 template <int NP>
@@ -87,6 +100,15 @@ __device__ __forceinline__ void split_store_a(uint32_t taddr_hi, const float (&v
 //   static __device__ void finish_a(const Params&, const uint8_t* extra, const Tile&,
 //                                   int kiter, int row, int k0, float (&v)[32])
 //        -> the block's transform, in place (runs after the loads have landed)
+//   static constexpr bool kStagedA; and when it is true:
+//   static __device__ void issue_a_box(const Params&, const Tile&, int kiter, int quarter,
+//                                      int khalf, uint32_t dst_smem, uint32_t bar)
+//        -> issues the TMA copy of the raw input the warp (quarter, khalf) needs for
+//           the stage into its slot, completing on bar (the caller arms it)
+//   static __device__ void read_a(const Params&, const uint8_t* extra, const Tile&,
+//                                 int kiter, int row, int k0, int lane, uint32_t box_smem,
+//                                 float (&v)[32])
+//        -> A[row][kiter*64 + k0 .. +32) from the landed slot, transform applied
 //   static __device__ const void* b_src(const Params&, const Tile&, int kiter)
 //        -> packed B image of the stage: NP parts of BN rows x 128 B, swizzled
 //   template <class Acquire>
@@ -99,18 +121,19 @@ __device__ __forceinline__ void split_store_a(uint32_t taddr_hi, const float (&v
 //           quarter (every lane executes the tcgen05.ld calls)
 template <class Prob, int NP>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const typename Prob::Params p, const GemmCfg cfg) {
+    gemm_kernel(const __grid_constant__ typename Prob::Params p, const GemmCfg cfg) {
     using Tile = typename Prob::Tile;
     constexpr int SA = (int)((kTmemCols - kTmemARing) / (32u * NP));   // A ring depth
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int SB = cfg.b_stages;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)SB * cfg.b_stage_bytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * kMaxStages + 5);
+    uint8_t* xslots = smem + (size_t)SB * cfg.b_stage_bytes;
+    const size_t x_bytes = (size_t)kProducerWarps * cfg.x_depth * cfg.x_box_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(xslots + x_bytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    uint8_t* extra = reinterpret_cast<uint8_t*>(smem) + (size_t)SB * cfg.b_stage_bytes +
-                     gemm_bookkeeping_bytes();
+    uint8_t* extra = reinterpret_cast<uint8_t*>(bars) + gemm_bookkeeping_bytes();
 
     const uint32_t bar0 = smem_u32(bars);
     auto a_full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
@@ -120,6 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acc_full = bar0 + 8u * (uint32_t)(4 * kMaxStages);
     const uint32_t acc_empty = acc_full + 8u;
     const uint32_t drain_bar = acc_full + 16u;
+    // A-source slot j of producer warp pw
+    auto x_full = [&](int pw, int j) {
+        return bar0 + 8u * (uint32_t)(4 * kMaxStages + 5 + pw * kMaxXDepth + j);
+    };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BN = cfg.BN;
@@ -137,6 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(acc_full, 1);           // MMA commit
         mbar_init(acc_empty, 4);          // one arrival per epilogue warp
         mbar_init(drain_bar, 1);
+        for (int pw = 0; pw < kProducerWarps; ++pw)
+            for (int j = 0; j < cfg.x_depth; ++j) mbar_init(x_full(pw, j), 1);   // expect_tx
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -236,12 +265,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quarter * 32 + lane;
         const int k0 = khalf * 32;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        // load cursor runs one stage ahead of the process cursor
-        int ltile = blockIdx.x, lk = 0;
-        int ptile = blockIdx.x, pk = 0;
-        Tile ltl{}, ptl{};
-        if (ltile < cfg.num_tiles) ltl = Prob::tile_info(p, ltile);
-        ptl = ltl;
         int sa = 0;
         uint32_t pha = 0;
         auto advance = [&](int& t, int& kk, Tile& tl) {
@@ -251,9 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t < cfg.num_tiles) tl = Prob::tile_info(p, t);
             }
         };
+        // Waits for a free A-ring stage, writes v into it and publishes it.
         // Returns false when the pipeline is being aborted.
-        auto process = [&](float (&v)[32]) -> bool {
-            Prob::finish_a(p, extra, ptl, pk, row, k0, v);
+        auto store_a = [&](const float (&v)[32]) -> bool {
             int w_ok = 1;
             if (lane == 0) w_ok = mbar_wait(a_empty(sa), pha ^ 1u, ctx, kSiteAEmpty);
             w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
@@ -266,25 +289,100 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full(sa));
             if (++sa == SA) { sa = 0; pha ^= 1u; }
-            advance(ptile, pk, ptl);
             return true;
         };
-        float v0[32], v1[32];
-        if (ltile < cfg.num_tiles) {
-            Prob::load_a(p, ltl, lk, row, k0, v0);
-            advance(ltile, lk, ltl);
-        }
-        while (ptile < cfg.num_tiles) {
-            if (ltile < cfg.num_tiles) {
-                Prob::load_a(p, ltl, lk, row, k0, v1);
-                advance(ltile, lk, ltl);
+        if constexpr (Prob::kStagedA) {
+            // Private ring of D slots; the copy cursor runs D stages ahead of
+            // the process cursor.  Bit j of iss_par / cons_par: parity of the
+            // copies issued into / consumed from slot j (they differ while a
+            // copy is in flight).
+            const int D = cfg.x_depth;
+            const int pw = warp - 2;
+            const uint32_t slot0 =
+                smem_u32(xslots + (size_t)pw * D * cfg.x_box_bytes);
+            int itile = blockIdx.x, ik = 0, islot = 0;
+            int ptile = blockIdx.x, pk = 0, pslot = 0;
+            Tile itl{}, ptl{};
+            if (itile < cfg.num_tiles) itl = Prob::tile_info(p, itile);
+            ptl = itl;
+            uint32_t iss_par = 0, cons_par = 0;
+            auto issue = [&]() {
+                if (itile >= cfg.num_tiles) return;
+                if (lane == 0) {
+                    const uint32_t bar = x_full(pw, islot);
+                    mbar_arrive_expect_tx(bar, cfg.x_box_bytes);
+                    Prob::issue_a_box(p, itl, ik, quarter, khalf,
+                                      slot0 + (uint32_t)islot * cfg.x_box_bytes, bar);
+                }
+                iss_par ^= 1u << islot;
+                advance(itile, ik, itl);
+                if (++islot == D) islot = 0;
+            };
+            for (int j = 0; j < D; ++j) issue();
+            bool ok = true;
+            while (ptile < cfg.num_tiles) {
+                const uint32_t par = (cons_par >> pslot) & 1u;
+                int w_ok = 1;
+                if (lane == 0) w_ok = mbar_wait(x_full(pw, pslot), par, ctx, kSiteFullX);
+                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+                if (!w_ok) {
+                    ok = false;
+                    break;
+                }
+                // The phase is complete (lane 0 saw it) and stays so until this
+                // warp refills the slot: every lane's own test succeeds at once
+                // and orders its reads after the copy.
+                (void)mbar_try_wait(x_full(pw, pslot), par);
+                float v[32];
+                Prob::read_a(p, extra, ptl, pk, row, k0, lane,
+                             slot0 + (uint32_t)pslot * cfg.x_box_bytes, v);
+                cons_par ^= 1u << pslot;
+                __syncwarp();
+                if (lane == 0) fence_proxy_async_smem();
+                issue();                          // refill this slot, D stages ahead
+                if (++pslot == D) pslot = 0;
+                if (!store_a(v)) {
+                    ok = false;
+                    break;
+                }
+                advance(ptile, pk, ptl);
             }
-            if (!process(v0) || ptile >= cfg.num_tiles) break;
+            if (!ok && lane == 0) {
+                // Let every copy still in flight land before the CTA can exit.
+                for (int j = 0; j < D; ++j)
+                    if (((iss_par ^ cons_par) >> j) & 1u)
+                        mbar_wait_drain(x_full(pw, j), (cons_par >> j) & 1u, 200000000ull);
+            }
+        } else {
+            // Raw values loaded into registers, one stage ahead.
+            int ltile = blockIdx.x, lk = 0;
+            int ptile = blockIdx.x, pk = 0;
+            Tile ltl{}, ptl{};
+            if (ltile < cfg.num_tiles) ltl = Prob::tile_info(p, ltile);
+            ptl = ltl;
+            auto process = [&](float (&v)[32]) -> bool {
+                Prob::finish_a(p, extra, ptl, pk, row, k0, v);
+                if (!store_a(v)) return false;
+                advance(ptile, pk, ptl);
+                return true;
+            };
+            float v0[32], v1[32];
             if (ltile < cfg.num_tiles) {
                 Prob::load_a(p, ltl, lk, row, k0, v0);
                 advance(ltile, lk, ltl);
             }
-            if (!process(v1)) break;
+            while (ptile < cfg.num_tiles) {
+                if (ltile < cfg.num_tiles) {
+                    Prob::load_a(p, ltl, lk, row, k0, v1);
+                    advance(ltile, lk, ltl);
+                }
+                if (!process(v0) || ptile >= cfg.num_tiles) break;
+                if (ltile < cfg.num_tiles) {
+                    Prob::load_a(p, ltl, lk, row, k0, v0);
+                    advance(ltile, lk, ltl);
+                }
+                if (!process(v1)) break;
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue

@@ -11,24 +11,37 @@
 namespace nrc {
 
 struct GemmPlan {
-    int BN, num_tiles, num_kiters, b_stages;
-    uint32_t b_stage_bytes, extra_bytes, smem_bytes;
+    int BN, num_tiles, num_kiters, b_stages, x_depth;
+    uint32_t b_stage_bytes, x_box_bytes, extra_bytes, smem_bytes;
 };
 
-// B ring depth: as many stages as fit in the opt-in shared memory next to the
-// bookkeeping and the block's extra bytes (at most kMaxStages).
+// Shared-memory split.  Register-loaded A: as many B stages as fit (at most
+// kMaxStages).  Staged A (x_box_bytes > 0, one slot per producer warp per
+// depth level): the deepest B ring (at most 4) that still leaves two slots per
+// warp, then as many slots as fit (at most kMaxXDepth).  b_stages < 2 or
+// x_depth < 2 (staged) means the problem does not fit.
 inline GemmPlan make_gemm_plan(int BN, int num_tiles, int num_kiters, int NP,
-                               uint32_t extra_bytes) {
+                               uint32_t extra_bytes, uint32_t x_box_bytes = 0) {
     GemmPlan g{};
     g.BN = BN;
     g.num_tiles = num_tiles;
     g.num_kiters = num_kiters;
     g.b_stage_bytes = (uint32_t)NP * (uint32_t)BN * 128u;
+    g.x_box_bytes = x_box_bytes;
     g.extra_bytes = extra_bytes;
     const uint32_t fixed = 1024u + gemm_bookkeeping_bytes() + extra_bytes;
-    g.b_stages = std::min<int>(kMaxStages, (int)((kMaxSmemBytes - fixed) / g.b_stage_bytes));
-    g.smem_bytes = 1024u + (uint32_t)g.b_stages * g.b_stage_bytes + gemm_bookkeeping_bytes() +
-                   extra_bytes;
+    const long long avail = (long long)kMaxSmemBytes - fixed;
+    if (x_box_bytes == 0) {
+        g.x_depth = 0;
+        g.b_stages = (int)std::min<long long>(kMaxStages, avail / g.b_stage_bytes);
+    } else {
+        const long long xset = (long long)kProducerWarps * x_box_bytes;
+        g.b_stages = (int)std::min<long long>(4, (avail - 2 * xset) / g.b_stage_bytes);
+        g.x_depth = (int)std::min<long long>(
+            kMaxXDepth, (avail - (long long)std::max(g.b_stages, 0) * g.b_stage_bytes) / xset);
+    }
+    g.smem_bytes = fixed + (uint32_t)std::max(g.b_stages, 0) * g.b_stage_bytes +
+                   (uint32_t)kProducerWarps * (uint32_t)std::max(g.x_depth, 0) * x_box_bytes;
     return g;
 }
 
@@ -36,6 +49,8 @@ template <class Prob, int NP>
 inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
                               const GemmPlan& pl, cudaStream_t stream) {
     if (pl.b_stages < 2) return NRC_ERR_UNSUPPORTED;
+    if (Prob::kStagedA != (pl.x_box_bytes > 0) || (Prob::kStagedA && pl.x_depth < 2))
+        return NRC_ERR_UNSUPPORTED;
     auto kern = gemm_kernel<Prob, NP>;
     // The opt-in shared-memory size is raised once per device and kernel
     // (to the maximum), so calls issue no host API work between launches.
@@ -55,6 +70,8 @@ inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
     cfg.num_kiters = pl.num_kiters;
     cfg.b_stages = pl.b_stages;
     cfg.b_stage_bytes = pl.b_stage_bytes;
+    cfg.x_depth = pl.x_depth;
+    cfg.x_box_bytes = pl.x_box_bytes;
     cfg.status = device_status_ptr();
     cfg.timeout_ns = wait_timeout_ns();
     if (cfg.status == nullptr) return NRC_ERR_CUDA;

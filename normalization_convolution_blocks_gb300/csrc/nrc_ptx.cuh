@@ -132,6 +132,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
         : "memory");
 }
 
+// Tiled tensor copy global -> shared of one 3-D box described by a tensor map
+// (kernel-parameter address), completion on an mbarrier.  Coordinates are
+// element indices, innermost first; parts of the box outside the tensor are
+// filled (zero or NaN, as the map says).  The innermost coordinate times the
+// element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void* tmap, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst_smem),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst_smem, const void* src,
                                               uint32_t bytes, uint32_t bar, uint64_t policy) {
     asm volatile(
@@ -286,6 +300,18 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
     __nv_bfloat162 l = __floats2bfloat162_rn(a - ah, b - bh);
     hi = *reinterpret_cast<uint32_t*>(&h);
     lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+// A bf16 in shared memory, widened to float.
+__device__ __forceinline__ float ld_shared_bf16(uint32_t addr) {
+    unsigned short u;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(u) : "r"(addr) : "memory");
+    return __uint_as_float((uint32_t)u << 16);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -82,6 +82,20 @@ def test_bf16_storage(C, d):
     assert_bf16(got, _oracle(inp), f"bf16 C{C} d{d}")
 
 
+# bf16 rows are gathered by TMA boxes when L * 2 bytes is a multiple of 16 and
+# loaded directly otherwise; both sides of that switch, with ragged tails,
+# channel counts off the 32/64 grid and taps reaching past both ends.
+@pytest.mark.parametrize("N,C,L,d", [
+    (2, 96, 296, 5),        # boxes; ragged tail, odd dilation (unaligned tap offsets)
+    (2, 96, 300, 5),        # direct loads (L*2 not a multiple of 16)
+    (1, 40, 136, 200),      # boxes; dilation > L: side taps all padding
+])
+def test_bf16_shapes(N, C, L, d):
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(N, C, L, d, seed=N * 100 + C + d, dtype=torch.bfloat16)
+    assert_bf16(_gpu(dev, inp), _oracle(inp), f"bf16 N{N} C{C} L{L} d{d}")
+
+
 def test_full_workload_fp32_sampled_rows():
     """The full-size workload (N=32 C=256 L=4096 d=128) in the bench's launch
     configuration, compared on 48 sampled output rows (all L positions)."""
