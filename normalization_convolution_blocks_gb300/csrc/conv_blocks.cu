@@ -9,9 +9,9 @@
 // in tensor memory by the prologue warps: the conv input for the tile's shifted
 // window, with BN+ReLU applied (block) and the zero padding applied after it,
 // split into bf16 hi/lo parts for fp32 storage.  When the rows of x are 16-byte
-// aligned, each prologue warp gathers its part of a tap's shifted window as a
-// TMA box (32 channels x 32 rows, start rounded down to 16 bytes) with
-// out-of-range rows filled by the copy itself; otherwise it loads x directly.
+// aligned, each stage's shifted window (64 channels x 128 rows of one tap,
+// start rounded down to 16 bytes) is gathered as one TMA box, out-of-range rows
+// filled by the copy itself; otherwise the prologue warps load x directly.
 // The B operand (weights) is repacked once per call into the exact
 // shared-memory image the MMA reads.
 #include <cuda_bf16.h>
@@ -47,7 +47,7 @@ __device__ __forceinline__ void store_f<__nv_bfloat16>(__nv_bfloat16* p, float v
 enum class ConvEpi { kResidual, kGroupStats };
 
 struct ConvParams {
-    CUtensorMap xmap;       // x as (L, Cin, N) boxes of (32 + 16/esize) x 32 x 1 (staged A)
+    CUtensorMap xmap;       // x as (L, Cin, N) boxes of (128 + 16/esize) x 64 x 1 (staged A)
     const void* x;          // (N, Cin, L)
     void* out;              // (N, Cout, L)
     int N, Cin, Cout, L;
@@ -104,8 +104,8 @@ struct ConvProblem {
     using Tile = ConvTile;
     static constexpr bool kStagedA = STAGED;
     static constexpr int kAlign = 16 / (int)sizeof(T);   // box starts on 16-byte boundaries
-    static constexpr int kBoxW = 32 + kAlign;             // rows (time positions) per box
-    static constexpr uint32_t kBoxBytes = (uint32_t)(kBoxW * 32 * sizeof(T));
+    static constexpr int kBoxW = kBM + kAlign;            // rows (time positions) per box
+    static constexpr uint32_t kBoxBytes = (uint32_t)(kBoxW * kBK * sizeof(T));
 
     static __device__ __forceinline__ Tile tile_info(const Params& p, int tile) {
         return conv_tile(p, tile);
@@ -164,24 +164,22 @@ struct ConvProblem {
         }
     }
 
-    // Staged A.  The warp's rows t0 + 32*quarter .. +32 read input rows from
-    // s = t0 + 32*quarter - pad + tap*dil; the box starts at s rounded down to
-    // the 16-byte boundary and the warp reads from offset s mod kAlign.  Rows
-    // outside [0, L) and channels past Cin come back as the map's fill: NaN
-    // when BN precedes the conv (max(NaN*scale + shift, 0) = 0, so the padding
-    // is applied after BN+ReLU, as the block defines it), zero otherwise.
-    static __device__ __forceinline__ int box_row0(const Params& p, const Tile& tl, int tap,
-                                                   int quarter) {
-        return tl.tt * kBM + quarter * 32 - p.pad + tap * p.dil;
+    // Staged A.  Tile rows t0 .. t0+128 read input rows from
+    // s = t0 - pad + tap*dil on; the stage's box starts at s rounded down to the
+    // 16-byte boundary and row r sits at offset r + s mod kAlign.  Rows outside
+    // [0, L) and channels past Cin come back as the map's fill: NaN when BN
+    // precedes the conv (max(NaN*scale + shift, 0) = 0, so the padding is
+    // applied after BN+ReLU, as the block defines it), zero otherwise.
+    static __device__ __forceinline__ int box_row0(const Params& p, const Tile& tl, int tap) {
+        return tl.tt * kBM - p.pad + tap * p.dil;
     }
 
     static __device__ __forceinline__ void issue_a_box(const Params& p, const Tile& tl,
-                                                       int kiter, int quarter, int khalf,
-                                                       uint32_t dst, uint32_t bar) {
+                                                       int kiter, uint32_t dst, uint32_t bar) {
         const int tap = kiter >= 2 * p.n_chunks ? 2 : (kiter >= p.n_chunks ? 1 : 0);
         const int chunk = kiter - tap * p.n_chunks;
-        const int s = box_row0(p, tl, tap, quarter);
-        tma_load_3d(dst, &p.xmap, s & ~(kAlign - 1), chunk * kBK + khalf * 32, tl.n, bar);
+        const int s = box_row0(p, tl, tap);
+        tma_load_3d(dst, &p.xmap, s & ~(kAlign - 1), chunk * kBK, tl.n, bar);
     }
 
     static __device__ __forceinline__ void read_a(const Params& p, const uint8_t* extra,
@@ -189,8 +187,8 @@ struct ConvProblem {
                                                   int lane, uint32_t box, float (&v)[32]) {
         const int tap = kiter >= 2 * p.n_chunks ? 2 : (kiter >= p.n_chunks ? 1 : 0);
         const int chunk = kiter - tap * p.n_chunks;
-        const int rem = box_row0(p, tl, tap, row >> 5) & (kAlign - 1);
-        const uint32_t a = box + (uint32_t)((lane + rem) * (int)sizeof(T));
+        const int rem = box_row0(p, tl, tap) & (kAlign - 1);
+        const uint32_t a = box + (uint32_t)((k0 * kBoxW + row + rem) * (int)sizeof(T));
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const uint32_t ai = a + (uint32_t)(i * kBoxW * (int)sizeof(T));
@@ -522,7 +520,7 @@ static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn,
 }
 
 // Tensor map of x for the staged A path: (L, Cin, N) with boxes of
-// (32 + 16/esize) rows x 32 channels x 1 sample.  Needs 16-byte aligned rows;
+// (128 + 16/esize) rows x 64 channels x 1 sample.  Needs 16-byte aligned rows;
 // false (use the register path) when they are not or the driver refuses.
 template <typename T>
 static bool make_x_map(ConvParams& p, const void* x, int N, int Cin, int L, bool nan_fill) {
@@ -530,7 +528,7 @@ static bool make_x_map(ConvParams& p, const void* x, int N, int Cin, int L, bool
     if (!aligned(x, 16) || ((size_t)L * es) % 16 != 0) return false;
     const uint64_t dims[3] = {(uint64_t)L, (uint64_t)Cin, (uint64_t)N};
     const uint64_t strides[2] = {(uint64_t)L * es, (uint64_t)Cin * L * es};
-    const uint32_t box[3] = {(uint32_t)(32 + 16 / es), 32u, 1u};
+    const uint32_t box[3] = {(uint32_t)(kBM + 16 / es), (uint32_t)kBK, 1u};
     return encode_tensor_map_3d(
         &p.xmap, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x,
         dims, strides, box, nan_fill);
@@ -542,7 +540,7 @@ template <typename T>
 static bool plan_conv_staged(ConvParams& p, ConvPlan& pl, int N, int Cin, int Cout, int L,
                              bool with_bn) {
     constexpr int NP = sizeof(T) == 4 ? 2 : 1;
-    constexpr uint32_t box_bytes = (uint32_t)((32 + 16 / sizeof(T)) * 32 * sizeof(T));
+    constexpr uint32_t box_bytes = (uint32_t)((kBM + 16 / sizeof(T)) * kBK * sizeof(T));
     if (make_x_map<T>(p, p.x, N, Cin, L, with_bn)) {
         pl = plan_conv(N, Cin, Cout, L, NP, with_bn, box_bytes);
         if (pl.g.b_stages >= 2 && pl.g.x_depth >= 2) return true;

@@ -5,10 +5,11 @@
 //   * A (the activation side) is produced by eight prologue warps: each block's
 //     own load-and-transform, split into bf16 parts and written straight into
 //     tensor memory with tcgen05.st; the MMA reads A from TMEM.  With a staged
-//     A source (Prob::kStagedA) every prologue warp first pulls its raw input
-//     box into a small private ring of shared-memory slots with tiled TMA
-//     copies (cp.async.bulk.tensor), D stages ahead, and transforms from there;
-//     otherwise it loads the raw values into registers one stage ahead.
+//     A source (Prob::kStagedA) one thread copies each stage's raw input box
+//     into a ring of D shared-memory slots with tiled TMA copies
+//     (cp.async.bulk.tensor) and the prologue warps transform from there;
+//     otherwise each prologue warp loads its raw values into registers one
+//     stage ahead.
 //   * B (the weight side) is bulk-copied (cp.async.bulk) from a pre-packed
 //     global image into a ring of shared-memory stages in the 128-byte swizzle
 //     layout the MMA's shared-memory descriptor expects.
@@ -21,14 +22,15 @@
 // v = hi + lo split in bf16): products exact to ~2^-16 relative, accumulated in
 // fp32.  bf16 storage runs one.
 //
-// Warp roles (448 threads):
+// Warp roles (480 threads):
 //   warp 0      B producer: one thread issues the bulk copies
 //   warp 1      allocates all 512 TMEM columns; one thread issues the MMAs
 //   warps 2-9   A producers: warp w owns TMEM lanes 32*(w%4).. (tile rows), K half (w-2)/4
 //   warps 10-13 epilogue: warp w drains TMEM lanes 32*(w%4)..
+//   warp 14     A-source copies (staged A): one thread issues the TMA boxes
 //
-// Shared memory: [B ring][A-source slots: 8 warps x D][barriers, TMEM slot,
-// abort flag][the block's extra bytes].
+// Shared memory: [B ring][A-source ring: D slots][barriers, TMEM slot, abort
+// flag][the block's extra bytes].
 //
 // TMEM columns: [0, BN) accumulator; [256, 512) A ring, stage s at
 // 256 + s*32*NP (hi part: 32 columns = 64 bf16 of K; then the lo part).
@@ -39,21 +41,21 @@
 
 namespace nrc {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kBM = 128;            // rows of a tile (MMA M)
 constexpr int kBK = 64;             // K elements per stage (one 128-byte swizzle row)
 constexpr int kUMMA_K = 16;         // K of one bf16 MMA
 constexpr int kMaxStages = 8;
 constexpr int kProducerWarps = 8;
-constexpr int kMaxXDepth = 4;       // A-source slots per producer warp (staged A)
-constexpr int kNumBars = 4 * kMaxStages + 5 + kProducerWarps * kMaxXDepth;
+constexpr int kMaxXDepth = 8;       // A-source ring slots (staged A)
+constexpr int kNumBars = 4 * kMaxStages + 5 + 2 * kMaxXDepth;
 constexpr int kMaxSmemBytes = 232448;          // 227 KB opt-in per CTA
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemARing = 256;           // first column of the A ring
 
 enum WaitSite : int {
     kSiteBEmpty = 1, kSiteAEmpty = 2, kSiteAccEmpty = 3, kSiteFullA = 4, kSiteFullB = 5,
-    kSiteAccFull = 6, kSiteFullX = 7
+    kSiteAccFull = 6, kSiteFullX = 7, kSiteEmptyX = 8
 };
 
 struct GemmCfg {
@@ -62,8 +64,8 @@ struct GemmCfg {
     int num_kiters;         // K stages per tile
     int b_stages;           // depth of the shared-memory B ring
     uint32_t b_stage_bytes; // NP * BN * 128
-    int x_depth;            // A-source slots per producer warp (0: A loaded to registers)
-    uint32_t x_box_bytes;   // bytes of one slot (a multiple of 128)
+    int x_depth;            // A-source ring slots (0: A loaded to registers)
+    uint32_t x_box_bytes;   // bytes of one slot: one stage's box (a multiple of 128)
     int* status;            // device status word
     unsigned long long timeout_ns;
 };
@@ -101,10 +103,10 @@ __device__ __forceinline__ void split_store_a(uint32_t taddr_hi, const float (&v
 //                                   int kiter, int row, int k0, float (&v)[32])
 //        -> the block's transform, in place (runs after the loads have landed)
 //   static constexpr bool kStagedA; and when it is true:
-//   static __device__ void issue_a_box(const Params&, const Tile&, int kiter, int quarter,
-//                                      int khalf, uint32_t dst_smem, uint32_t bar)
-//        -> issues the TMA copy of the raw input the warp (quarter, khalf) needs for
-//           the stage into its slot, completing on bar (the caller arms it)
+//   static __device__ void issue_a_box(const Params&, const Tile&, int kiter,
+//                                      uint32_t dst_smem, uint32_t bar)
+//        -> issues the TMA copy of the raw input of the whole stage into a slot,
+//           completing on bar (the caller arms it)
 //   static __device__ void read_a(const Params&, const uint8_t* extra, const Tile&,
 //                                 int kiter, int row, int k0, int lane, uint32_t box_smem,
 //                                 float (&v)[32])
@@ -125,11 +127,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     using Tile = typename Prob::Tile;
     constexpr int SA = (int)((kTmemCols - kTmemARing) / (32u * NP));   // A ring depth
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned base, derived by pointer arithmetic so every pointer
+    // into it stays in the shared state space (native shared loads/stores).
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int SB = cfg.b_stages;
     uint8_t* xslots = smem + (size_t)SB * cfg.b_stage_bytes;
-    const size_t x_bytes = (size_t)kProducerWarps * cfg.x_depth * cfg.x_box_bytes;
+    const size_t x_bytes = (size_t)cfg.x_depth * cfg.x_box_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(xslots + x_bytes);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -143,9 +146,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acc_full = bar0 + 8u * (uint32_t)(4 * kMaxStages);
     const uint32_t acc_empty = acc_full + 8u;
     const uint32_t drain_bar = acc_full + 16u;
-    // A-source slot j of producer warp pw
-    auto x_full = [&](int pw, int j) {
-        return bar0 + 8u * (uint32_t)(4 * kMaxStages + 5 + pw * kMaxXDepth + j);
+    // A-source slot j: full (TMA complete_tx) / empty (producer warps)
+    auto x_full = [&](int j) { return bar0 + 8u * (uint32_t)(4 * kMaxStages + 5 + j); };
+    auto x_empty = [&](int j) {
+        return bar0 + 8u * (uint32_t)(4 * kMaxStages + 5 + kMaxXDepth + j);
     };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -164,8 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(acc_full, 1);           // MMA commit
         mbar_init(acc_empty, 4);          // one arrival per epilogue warp
         mbar_init(drain_bar, 1);
-        for (int pw = 0; pw < kProducerWarps; ++pw)
-            for (int j = 0; j < cfg.x_depth; ++j) mbar_init(x_full(pw, j), 1);   // expect_tx
+        for (int j = 0; j < cfg.x_depth; ++j) {
+            mbar_init(x_full(j), 1);                  // the issuer's arrive.expect_tx
+            mbar_init(x_empty(j), kProducerWarps);    // one arrival per A-producer warp
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -292,66 +298,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
         if constexpr (Prob::kStagedA) {
-            // Private ring of D slots; the copy cursor runs D stages ahead of
-            // the process cursor.  Bit j of iss_par / cons_par: parity of the
-            // copies issued into / consumed from slot j (they differ while a
-            // copy is in flight).
+            // Stage k's raw input sits in slot k % D once x_full completes; the
+            // warp reads its 32 rows x 32 channels and releases the slot.
             const int D = cfg.x_depth;
-            const int pw = warp - 2;
-            const uint32_t slot0 =
-                smem_u32(xslots + (size_t)pw * D * cfg.x_box_bytes);
-            int itile = blockIdx.x, ik = 0, islot = 0;
+            const uint32_t slot0 = smem_u32(xslots);
             int ptile = blockIdx.x, pk = 0, pslot = 0;
-            Tile itl{}, ptl{};
-            if (itile < cfg.num_tiles) itl = Prob::tile_info(p, itile);
-            ptl = itl;
-            uint32_t iss_par = 0, cons_par = 0;
-            auto issue = [&]() {
-                if (itile >= cfg.num_tiles) return;
-                if (lane == 0) {
-                    const uint32_t bar = x_full(pw, islot);
-                    mbar_arrive_expect_tx(bar, cfg.x_box_bytes);
-                    Prob::issue_a_box(p, itl, ik, quarter, khalf,
-                                      slot0 + (uint32_t)islot * cfg.x_box_bytes, bar);
-                }
-                iss_par ^= 1u << islot;
-                advance(itile, ik, itl);
-                if (++islot == D) islot = 0;
-            };
-            for (int j = 0; j < D; ++j) issue();
-            bool ok = true;
+            uint32_t pphase = 0;
+            Tile ptl{};
+            if (ptile < cfg.num_tiles) ptl = Prob::tile_info(p, ptile);
             while (ptile < cfg.num_tiles) {
-                const uint32_t par = (cons_par >> pslot) & 1u;
                 int w_ok = 1;
-                if (lane == 0) w_ok = mbar_wait(x_full(pw, pslot), par, ctx, kSiteFullX);
+                if (lane == 0) w_ok = mbar_wait(x_full(pslot), pphase, ctx, kSiteFullX);
                 w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-                if (!w_ok) {
-                    ok = false;
-                    break;
-                }
-                // The phase is complete (lane 0 saw it) and stays so until this
-                // warp refills the slot: every lane's own test succeeds at once
-                // and orders its reads after the copy.
-                (void)mbar_try_wait(x_full(pw, pslot), par);
+                if (!w_ok) break;
+                // The phase is complete (lane 0 saw it) and stays so until the
+                // slot is released: every lane's own test succeeds at once and
+                // orders its reads after the copy.
+                (void)mbar_try_wait(x_full(pslot), pphase);
                 float v[32];
                 Prob::read_a(p, extra, ptl, pk, row, k0, lane,
                              slot0 + (uint32_t)pslot * cfg.x_box_bytes, v);
-                cons_par ^= 1u << pslot;
                 __syncwarp();
-                if (lane == 0) fence_proxy_async_smem();
-                issue();                          // refill this slot, D stages ahead
-                if (++pslot == D) pslot = 0;
-                if (!store_a(v)) {
-                    ok = false;
-                    break;
-                }
+                if (lane == 0) mbar_arrive(x_empty(pslot));
+                if (++pslot == D) { pslot = 0; pphase ^= 1u; }
+                if (!store_a(v)) break;
                 advance(ptile, pk, ptl);
-            }
-            if (!ok && lane == 0) {
-                // Let every copy still in flight land before the CTA can exit.
-                for (int j = 0; j < D; ++j)
-                    if (((iss_par ^ cons_par) >> j) & 1u)
-                        mbar_wait_drain(x_full(pw, j), (cons_par >> j) & 1u, 200000000ull);
             }
         } else {
             // Raw values loaded into registers, one stage ahead.
@@ -382,6 +353,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     advance(ltile, lk, ltl);
                 }
                 if (!process(v1)) break;
+            }
+        }
+    } else if (warp == 14) {
+        // ------------------------------------------------------------ A-source copies
+        if constexpr (Prob::kStagedA) {
+            if (lane == 0) {
+                const int D = cfg.x_depth;
+                const uint32_t slot0 = smem_u32(xslots);
+                int slot = 0;
+                uint32_t phase = 0;
+                uint32_t armed = 0, armed_par = 0;     // bit j: copy in flight / its parity
+                bool ok = true;
+                for (int tile = blockIdx.x; ok && tile < cfg.num_tiles; tile += gridDim.x) {
+                    const Tile tl = Prob::tile_info(p, tile);
+                    for (int k = 0; k < cfg.num_kiters; ++k) {
+                        if (!mbar_wait(x_empty(slot), phase ^ 1u, ctx, kSiteEmptyX)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(x_full(slot), cfg.x_box_bytes);
+                        Prob::issue_a_box(p, tl, k, slot0 + (uint32_t)slot * cfg.x_box_bytes,
+                                          x_full(slot));
+                        armed |= 1u << slot;
+                        armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
+                        if (++slot == D) { slot = 0; phase ^= 1u; }
+                    }
+                }
+                if (!ok) {
+                    // Let every copy still in flight land before the CTA can exit.
+                    for (int j = 0; j < D; ++j)
+                        if ((armed >> j) & 1u)
+                            mbar_wait_drain(x_full(j), (armed_par >> j) & 1u, 200000000ull);
+                }
             }
         }
     } else {

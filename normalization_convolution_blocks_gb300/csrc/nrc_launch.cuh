@@ -16,10 +16,10 @@ struct GemmPlan {
 };
 
 // Shared-memory split.  Register-loaded A: as many B stages as fit (at most
-// kMaxStages).  Staged A (x_box_bytes > 0, one slot per producer warp per
-// depth level): the deepest B ring (at most 4) that still leaves two slots per
-// warp, then as many slots as fit (at most kMaxXDepth).  b_stages < 2 or
-// x_depth < 2 (staged) means the problem does not fit.
+// kMaxStages).  Staged A (x_box_bytes > 0, one slot per stage): the deepest B
+// ring (at most 4) that still leaves two A-source slots, then as many slots as
+// fit (at most kMaxXDepth).  b_stages < 2 or x_depth < 2 (staged) means the
+// problem does not fit.
 inline GemmPlan make_gemm_plan(int BN, int num_tiles, int num_kiters, int NP,
                                uint32_t extra_bytes, uint32_t x_box_bytes = 0) {
     GemmPlan g{};
@@ -35,13 +35,13 @@ inline GemmPlan make_gemm_plan(int BN, int num_tiles, int num_kiters, int NP,
         g.x_depth = 0;
         g.b_stages = (int)std::min<long long>(kMaxStages, avail / g.b_stage_bytes);
     } else {
-        const long long xset = (long long)kProducerWarps * x_box_bytes;
-        g.b_stages = (int)std::min<long long>(4, (avail - 2 * xset) / g.b_stage_bytes);
+        g.b_stages = (int)std::min<long long>(4, (avail - 2LL * x_box_bytes) / g.b_stage_bytes);
         g.x_depth = (int)std::min<long long>(
-            kMaxXDepth, (avail - (long long)std::max(g.b_stages, 0) * g.b_stage_bytes) / xset);
+            kMaxXDepth, (avail - (long long)std::max(g.b_stages, 0) * g.b_stage_bytes) /
+                            (long long)x_box_bytes);
     }
     g.smem_bytes = fixed + (uint32_t)std::max(g.b_stages, 0) * g.b_stage_bytes +
-                   (uint32_t)kProducerWarps * (uint32_t)std::max(g.x_depth, 0) * x_box_bytes;
+                   (uint32_t)std::max(g.x_depth, 0) * x_box_bytes;
     return g;
 }
 
