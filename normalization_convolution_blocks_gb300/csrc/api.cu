@@ -76,7 +76,7 @@ EncodeTiledFn encode_tiled_fn() {
 
 bool encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                           const uint64_t dims[3], const uint64_t strides[2],
-                          const uint32_t box[3], bool nan_fill) {
+                          const uint32_t box[3], bool nan_fill, bool swizzle128) {
     const EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     const cuuint64_t gdim[3] = {dims[0], dims[1], dims[2]};
@@ -84,7 +84,8 @@ bool encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const voi
     const cuuint32_t bdim[3] = {box[0], box[1], box[2]};
     const cuuint32_t estride[3] = {1, 1, 1};
     return fn(map, dtype, 3, const_cast<void*>(base), gdim, gstride, bdim, estride,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               nan_fill ? CU_TENSOR_MAP_FLOAT_OOB_FILL_NAN_REQUEST_ZERO_FMA
                        : CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

@@ -4,7 +4,10 @@
 // weight, converted to bf16 hi/lo by the prologue warps straight from fp32, so
 // the large weight is never rewritten), tile columns are BN batch rows b (B =
 // x, split into bf16 hi/lo once per call into the shared-memory image).
-// D[j][b] = y[b][j] - lin_bias[j].  With features on TMEM lanes, each thread
+// D[j][b] = y[b][j] - lin_bias[j].  When W's rows are 16-byte aligned, each
+// stage's 128 x 64 block of W is copied by TMA (two 32-wide boxes in the
+// 128-byte swizzle, so a lane reading its own row is bank-conflict free) and
+// the prologue warps convert it from shared memory.  With features on TMEM lanes, each thread
 // owns one column j of y: its epilogue stores y (coalesced across the warp)
 // and keeps the column's (count, mean, M2) over the tile's batch rows, so the
 // batch statistics need no cross-thread reduction.
@@ -22,6 +25,7 @@
 namespace nrc {
 
 struct LinearParams {
+    CUtensorMap wmap;        // W as (IN, OUT, 1) in 32 x 128 x 1 boxes, 128B-swizzled
     const float* W;          // (OUT, IN)
     const uint8_t* xpack;    // packed x image
     float* out;              // (B, OUT): receives y
@@ -36,10 +40,12 @@ struct LinearTile {
     int jt, bt;
 };
 
+template <bool STAGED>
 struct LinearProblem {
     using Params = LinearParams;
     using Tile = LinearTile;
-    static constexpr bool kStagedA = false;
+    static constexpr bool kStagedA = STAGED;
+    static constexpr uint32_t kBoxBytes = 2u * 128u * 128u;   // two 32-float x 128-row boxes
 
     // Tiles of one feature block are adjacent, so the CTAs reading the same
     // weight rows run together and the weight is fetched from HBM once.
@@ -77,6 +83,29 @@ struct LinearProblem {
 
     static __device__ __forceinline__ void finish_a(const Params&, const uint8_t*, const Tile&,
                                                     int, int, int, float (&)[32]) {}
+
+    // Staged A: K columns kiter*64 .. +32 and +32 .. +64 of rows jt*128 .. +128
+    // as two boxes; rows past OUT and columns past IN are zero.
+    static __device__ __forceinline__ void issue_a_box(const Params& p, const Tile& tl,
+                                                       int kiter, uint32_t dst, uint32_t bar) {
+        tma_load_3d(dst, &p.wmap, kiter * kBK, tl.jt * kBM, 0, bar);
+        tma_load_3d(dst + kBoxBytes / 2, &p.wmap, kiter * kBK + 32, tl.jt * kBM, 0, bar);
+    }
+
+    static __device__ __forceinline__ void read_a(const Params&, const uint8_t*, const Tile&,
+                                                  int, int row, int k0, int, uint32_t box,
+                                                  float (&v)[32]) {
+        const uint32_t rb = box + (uint32_t)(k0 / 32) * (kBoxBytes / 2) + (uint32_t)row * 128u;
+        const uint32_t sw = (uint32_t)(row & 7);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float4 q = ld_shared_v4f(rb + (((uint32_t)c ^ sw) << 4));
+            v[4 * c] = q.x;
+            v[4 * c + 1] = q.y;
+            v[4 * c + 2] = q.z;
+            v[4 * c + 3] = q.w;
+        }
+    }
 
     static __device__ __forceinline__ const void* b_src(const Params& p, const Tile& tl,
                                                         int kiter) {
@@ -244,14 +273,15 @@ struct LinearPlan {
     size_t xpack_bytes, partials_off, colp_off, total;
 };
 
-static LinearPlan plan_linear(int B, int IN, int OUT) {
+static LinearPlan plan_linear(int B, int IN, int OUT, uint32_t x_box_bytes = 0) {
     LinearPlan pl{};
     const int BN = B <= 256 ? ((B + 15) / 16) * 16 : 256;
     pl.n_bt = ceil_div(B, BN);
     pl.n_jt = ceil_div(OUT, kBM);
     const int n_kiters = ceil_div(IN, kBK);
     const long long tiles = (long long)pl.n_jt * pl.n_bt;
-    pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), n_kiters, 2, 0);
+    pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), n_kiters, 2, 0,
+                          x_box_bytes);
     pl.xpack_bytes = (size_t)pl.n_bt * n_kiters * 2 * BN * 128;
     pl.partials_off = (pl.xpack_bytes + 255) & ~(size_t)255;
     pl.colp_off = (pl.partials_off + (size_t)pl.n_bt * OUT * sizeof(float4) + 255) & ~(size_t)255;
@@ -287,7 +317,7 @@ extern "C" nrc_status nrc_linear_bn_swish(
     if (ranges_overlap(x, (size_t)B * in_f * 4, out, (size_t)B * out_f * 4))
         return NRC_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return NRC_ERR_ALIGNMENT;
-    const LinearPlan pl = plan_linear(B, in_f, out_f);
+    LinearPlan pl = plan_linear(B, in_f, out_f);
     if (workspace_bytes < pl.total) return NRC_ERR_WORKSPACE;
     if ((long long)pl.n_jt * pl.n_bt >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
 
@@ -307,6 +337,21 @@ extern "C" nrc_status nrc_linear_bn_swish(
     p.n_kiters = pl.g.num_kiters;
     p.BN = pl.g.BN;
     p.vec_ok = (in_f % 4 == 0) && aligned(lin_weight, 16);
+    // Staged A when W's rows are 16-byte aligned and the driver takes the map.
+    bool staged = false;
+    if (p.vec_ok) {
+        const uint64_t dims[3] = {(uint64_t)in_f, (uint64_t)out_f, 1};
+        const uint64_t strides[2] = {(uint64_t)in_f * 4, (uint64_t)in_f * 4 * out_f};
+        const uint32_t box[3] = {32u, (uint32_t)kBM, 1u};
+        if (encode_tensor_map_3d(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, lin_weight, dims,
+                                 strides, box, false, true)) {
+            const LinearPlan ps = plan_linear(B, in_f, out_f, LinearProblem<true>::kBoxBytes);
+            if (ps.g.b_stages >= 2 && ps.g.x_depth >= 2) {
+                pl = ps;
+                staged = true;
+            }
+        }
+    }
     float* colp = reinterpret_cast<float*>(ws + pl.colp_off);
 
     const size_t units = (size_t)pl.n_bt * pl.g.num_kiters * pl.g.BN * 8;
@@ -316,7 +361,8 @@ extern "C" nrc_status nrc_linear_bn_swish(
             x, ws, B, in_f, pl.g.BN, pl.n_bt, pl.g.num_kiters);
     }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
-    nrc_status s = launch_gemm<LinearProblem, 2>("linear_gemm", p, pl.g, st);
+    nrc_status s = staged ? launch_gemm<LinearProblem<true>, 2>("linear_gemm", p, pl.g, st)
+                          : launch_gemm<LinearProblem<false>, 2>("linear_gemm", p, pl.g, st);
     if (s != NRC_OK) return s;
     {
         TraceScope ts("bn_finalize", st);

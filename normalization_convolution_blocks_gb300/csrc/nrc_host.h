@@ -20,11 +20,14 @@ int device_sm_count();
 // Encodes a 3-D tiled tensor map (dims and box innermost first, strides in
 // bytes of dims 1 and 2) through the driver's cuTensorMapEncodeTiled, reached
 // via the runtime's entry-point query so the library does not link libcuda.
-// nan_fill: out-of-bounds elements read as NaN instead of zero.  Returns false
-// when the driver rejects the map or the entry point is unavailable.
+// nan_fill: out-of-bounds elements read as NaN instead of zero; swizzle128: the
+// box lands in shared memory in the 128-byte swizzle (16-byte chunk c of 128-byte
+// row r at chunk c ^ (r mod 8); box rows of exactly 128 bytes, destination
+// 1024-byte aligned).  Returns false when the driver rejects the map or the
+// entry point is unavailable.
 bool encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                           const uint64_t dims[3], const uint64_t strides[2],
-                          const uint32_t box[3], bool nan_fill);
+                          const uint32_t box[3], bool nan_fill, bool swizzle128 = false);
 
 inline bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);

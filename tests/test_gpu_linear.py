@@ -40,6 +40,7 @@ def _check(got, ref, what):
     (2, 64, 32, True),        # smallest training batch
     (300, 520, 200, True),    # two batch tiles, ragged
     (1024, 1024, 256, True),
+    (33, 37, 50, True),       # in_features % 4 != 0: W rows loaded directly, not by TMA
 ])
 def test_training_shapes(B, IN, OUT, affine):
     dev = need_gpu()
