@@ -60,7 +60,8 @@ struct ConvParams {
     int bias_off;           // float offset of the staged bias in the extra smem
     const uint8_t* wpack;   // packed weight image
     // group statistics (conv + GroupNorm)
-    float4* partials;       // [(n*G + g) * n_tt * 4 + tt*4 + quarter] = (count, mean, M2, 0)
+    float2* partials;       // [((n*G + g) * n_tt + tt) * 128 + row] = (mean, M2) of the
+                            // row's cpg values (count cpg, or 0 for rows past L)
     int G, cpg;
 };
 
@@ -80,7 +81,9 @@ __device__ __forceinline__ ConvTile conv_tile(const ConvParams& p, int tile) {
 
 // Warp-level merge of (count, mean, M2) triples (Chan et al.'s pairwise
 // update); every lane ends with the total.  Lanes with count 0 contribute
-// nothing.
+// nothing.  kFast: the weight nb/nab by the fast division intrinsic (a few ulp;
+// both are small exact counts), for the per-tile statistics in the epilogue.
+template <bool kFast = false>
 __device__ __forceinline__ void warp_merge_stats(float& cnt, float& mean, float& m2) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -90,11 +93,35 @@ __device__ __forceinline__ void warp_merge_stats(float& cnt, float& mean, float&
         const float nab = cnt + nb;
         if (nab > 0.f) {
             const float delta = mb - mean;
-            const float fb = nb / nab;
+            const float fb = kFast ? __fdividef(nb, nab) : nb / nab;
             mean = mean + delta * fb;
             m2 = m2 + qb + delta * delta * cnt * fb;
             cnt = nab;
         }
+    }
+}
+
+// GroupNorm statistics of one row over a 16-channel chunk holding 16/CPG whole
+// groups (CPG divides 16): for each group its (mean, M2) over the row's CPG
+// values, two-pass in registers, zero for a row outside [0, L) (tw = 0).
+// Groups at or past n (channels of the chunk that exist) are skipped.
+template <int CPG>
+__device__ __forceinline__ void gn_chunk_stats(const float (&v)[16], int n, float tw,
+                                               float2* part, size_t group_stride) {
+#pragma unroll
+    for (int j = 0; j < 16 / CPG; ++j) {
+        if (j * CPG >= n) break;
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < CPG; ++i) s += v[j * CPG + i];
+        const float m = s * (1.0f / CPG);
+        float q = 0.f;
+#pragma unroll
+        for (int i = 0; i < CPG; ++i) {
+            const float d = v[j * CPG + i] - m;
+            q = fmaf(d, d, q);
+        }
+        part[(size_t)j * group_stride] = make_float2(m * tw, q * tw);
     }
 }
 
@@ -307,7 +334,7 @@ struct ConvProblem {
                 if (cc + 48 < BN) emit(cc + 48, r3);
             }
         } else {
-            // y -> out, and per-(n, group, t tile, warp) statistics of y.  A
+            // y -> out, and per-(n, group, t tile, row) statistics of y.  A
             // group's channels are contiguous.  Each run of a group inside a
             // 16-channel chunk is reduced two-pass in registers (count, mean,
             // M2), folded into the group's running triple with Chan's update,
@@ -317,6 +344,18 @@ struct ConvProblem {
             const int ovalid = p.Cout - obase;
             float cnt = 0.f, mean = 0.f, m2 = 0.f;
             const float tw = t_ok ? 1.f : 0.f;
+            // first channel of the group after the current one (tiles hold whole
+            // groups, so this starts at obase + cpg and steps by cpg)
+            int gend = obase + p.cpg;
+            // sum of the 16 values selected by [lo, hi), as a 4-level tree
+            auto tree16 = [](const float (&a)[16]) {
+                float b[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) b[i] = a[2 * i] + a[2 * i + 1];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) b[i] = b[2 * i] + b[2 * i + 1];
+                return (b[0] + b[1]) + (b[2] + b[3]);
+            };
             for (int cc = 0; cc < BN && cc < ovalid; cc += 16) {
                 float v[16];
                 tmem_ld16(taddr + (uint32_t)cc, v);
@@ -341,39 +380,53 @@ struct ConvProblem {
                     for (int i = 0; i < 16; ++i)
                         if (t_ok && i < n) store_f<T>(op + (size_t)i * p.L, v[i]);
                 }
+                if (p.cpg <= 16 && 16 % p.cpg == 0) {
+                    // whole groups inside the chunk: group (obase + cc)/cpg + j
+                    const size_t gstride = (size_t)p.n_tt * kBM;
+                    float2* part = p.partials +
+                                   ((size_t)(tl.n * p.G + (obase + cc) / p.cpg) * p.n_tt + tl.tt) *
+                                       kBM +
+                                   quarter * 32 + lane;
+                    switch (p.cpg) {
+                        case 1: gn_chunk_stats<1>(v, n, tw, part, gstride); break;
+                        case 2: gn_chunk_stats<2>(v, n, tw, part, gstride); break;
+                        case 4: gn_chunk_stats<4>(v, n, tw, part, gstride); break;
+                        case 8: gn_chunk_stats<8>(v, n, tw, part, gstride); break;
+                        default: gn_chunk_stats<16>(v, n, tw, part, gstride); break;
+                    }
+                    continue;
+                }
                 // runs [i0, i1) of one group inside this chunk
                 int i0 = 0;
                 while (i0 < n) {
-                    const int o0 = obase + cc + i0;
-                    const int gend = (o0 / p.cpg + 1) * p.cpg;        // first channel of next group
                     const int i1 = min(n, gend - (obase + cc));
-                    float s = 0.f;
+                    float sel[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) s += (i >= i0 && i < i1) ? v[i] : 0.f;
+                    for (int i = 0; i < 16; ++i) sel[i] = (i >= i0 && i < i1) ? v[i] : 0.f;
                     const float k = (float)(i1 - i0);
-                    const float sm = s / k;
-                    float sq = 0.f;
+                    const float sm = __fdividef(tree16(sel), k);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const float d = (i >= i0 && i < i1) ? v[i] - sm : 0.f;
-                        sq = fmaf(d, d, sq);
+                        sel[i] = d * d;
                     }
+                    const float sq = tree16(sel);
                     const float kb = k * tw;                           // this run's count
                     const float nab = cnt + kb;
                     if (nab > 0.f) {
                         const float delta = sm - mean;
-                        const float fb = kb / nab;
+                        const float fb = __fdividef(kb, nab);
                         mean += delta * fb;
                         m2 += sq * tw + delta * delta * cnt * fb;
                         cnt = nab;
                     }
                     if (obase + cc + i1 == gend) {                     // group complete
-                        warp_merge_stats(cnt, mean, m2);
-                        if (lane == 0) {
-                            const int g = o0 / p.cpg;
-                            p.partials[((size_t)(tl.n * p.G + g) * p.n_tt + tl.tt) * 4 + quarter] =
-                                make_float4(cnt, mean, m2, 0.f);
-                        }
+                        // this row's (mean, M2) over the group's channels; the
+                        // rows of the tile are merged by the finalize kernel
+                        const int g = gend / p.cpg - 1;
+                        gend += p.cpg;
+                        p.partials[((size_t)(tl.n * p.G + g) * p.n_tt + tl.tt) * kBM +
+                                   quarter * 32 + lane] = make_float2(mean, m2);
                         cnt = 0.f;
                         mean = 0.f;
                         m2 = 0.f;
@@ -433,39 +486,58 @@ __global__ void pack_conv_weight_kernel(const T* __restrict__ w, uint8_t* __rest
 }
 
 // ---------------------------------------------------------------------------
-// GroupNorm finalize + normalize, one CTA per (n, group): merge the partial
-// (count, mean, M2) of the group in a fixed order, then
+// GroupNorm finalize + normalize, one CTA per (n, group): merge the group's
+// per-row partial (mean, M2) over its n_tt * 128 rows (count cpg per row inside
+// [0, T), 0 past it) in a fixed order -- each thread a strided subset, then the
+// warps, then the CTA -- and apply
 // out = (y - mean) * rsqrt(var + eps) * gamma + beta in place over the group's
 // contiguous (cpg x T) block.
 // ---------------------------------------------------------------------------
 __global__ void groupnorm_finalize_normalize_kernel(float* __restrict__ out,
-                                                    const float4* __restrict__ partials,
-                                                    int n_part, int Cout, int T, int G,
+                                                    const float2* __restrict__ partials,
+                                                    int n_tt, int Cout, int T, int G,
                                                     const float* __restrict__ gamma,
                                                     const float* __restrict__ beta, float eps) {
     const int ng = blockIdx.x;
     const int g = ng % G;
     const int cpg = Cout / G;
+    const int n_part = n_tt * kBM;
     __shared__ float s_mean, s_inv;
-    if (threadIdx.x < 32) {
-        float cnt = 0.f, mean = 0.f, m2 = 0.f;
-        for (int i = threadIdx.x; i < n_part; i += 32) {
-            const float4 q = partials[(size_t)ng * n_part + i];
-            const float nab = cnt + q.x;
-            if (nab > 0.f) {
-                const float delta = q.y - mean;
-                const float fb = q.x / nab;
-                mean += delta * fb;
-                m2 += q.z + delta * delta * cnt * fb;
-                cnt = nab;
-            }
+    __shared__ float s_w[3][32];
+    {
+    float cnt = 0.f, mean = 0.f, m2 = 0.f;
+    for (int i = threadIdx.x; i < n_part; i += blockDim.x) {
+        const float2 q = partials[(size_t)ng * n_part + i];
+        const float nb = (i < T) ? (float)cpg : 0.f;        // row i of the sample
+        const float nab = cnt + nb;
+        if (nab > 0.f) {
+            const float delta = q.x - mean;
+            const float fb = nb / nab;
+            mean += delta * fb;
+            m2 += q.y + delta * delta * cnt * fb;
+            cnt = nab;
         }
+    }
+    warp_merge_stats(cnt, mean, m2);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        s_w[0][warp] = cnt;
+        s_w[1][warp] = mean;
+        s_w[2][warp] = m2;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = (int)(blockDim.x >> 5);
+        cnt = lane < nw ? s_w[0][lane] : 0.f;
+        mean = lane < nw ? s_w[1][lane] : 0.f;
+        m2 = lane < nw ? s_w[2][lane] : 0.f;
         warp_merge_stats(cnt, mean, m2);
-        if (threadIdx.x == 0) {
+        if (lane == 0) {
             const float var = fmaxf(m2 / cnt, 0.f);   // biased variance
             s_mean = mean;
             s_inv = 1.0f / sqrtf(var + eps);
         }
+    }
     }
     __syncthreads();
     const float mean = s_mean, inv = s_inv;
@@ -641,7 +713,7 @@ extern "C" size_t nrc_conv1d_groupnorm_workspace_size(int N, int C_in, int C_out
                                                       int num_groups) {
     if (N <= 0 || C_in <= 0 || C_out <= 0 || T <= 0 || num_groups <= 0) return 0;
     const ConvPlan pl = plan_conv(N, C_in, C_out, T, 2, false);
-    return gn_partials_offset(pl) + (size_t)N * num_groups * pl.n_tt * 4 * sizeof(float4);
+    return gn_partials_offset(pl) + (size_t)N * num_groups * pl.n_tt * kBM * sizeof(float2);
 }
 
 extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, int C_in, int C_out,
@@ -689,7 +761,7 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     p.bias = conv_bias;
     p.bias_off = 0;
     p.wpack = ws;
-    p.partials = reinterpret_cast<float4*>(ws + gn_partials_offset(pl));
+    p.partials = reinterpret_cast<float2*>(ws + gn_partials_offset(pl));
     p.G = num_groups;
     p.cpg = cpg;
     const size_t units = pl.wpack_bytes / 16 / 2;
@@ -708,7 +780,7 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     {
         TraceScope ts("groupnorm_finalize_normalize", st);
         groupnorm_finalize_normalize_kernel<<<N * num_groups, 256, 0, st>>>(
-            out, p.partials, pl.n_tt * 4, C_out, T, num_groups, gn_gamma, gn_beta, eps);
+            out, p.partials, pl.n_tt, C_out, T, num_groups, gn_gamma, gn_beta, eps);
     }
     return cuda_status(cudaGetLastError());
 }

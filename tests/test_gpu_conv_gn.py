@@ -37,6 +37,9 @@ def test_full_workload():
     (2, 32, 512, 300, 32),    # two output tiles, 16 channels per group
     (1, 16, 256, 128, 1),     # one group spanning the whole tile
     (1, 16, 256, 130, 256),   # one channel per group
+    (2, 24, 48, 136, 24),     # 2 channels per group
+    (1, 40, 64, 200, 16),     # 4 channels per group
+    (2, 70, 96, 264, 8),      # 12 channels per group: groups cross 16-channel chunks
 ])
 def test_shapes(N, Cin, Cout, T, G):
     dev = need_gpu()
