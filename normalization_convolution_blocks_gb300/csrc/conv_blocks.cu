@@ -542,26 +542,24 @@ __global__ void groupnorm_finalize_normalize_kernel(float* __restrict__ out,
     __syncthreads();
     const float mean = s_mean, inv = s_inv;
     float* base = out + (size_t)ng * cpg * T;      // channels g*cpg.. of sample n
-    const size_t cnt = (size_t)cpg * T;
-    if ((T & 3) == 0) {
-        float4* b4 = reinterpret_cast<float4*>(base);
-        for (size_t i = threadIdx.x; i < cnt / 4; i += blockDim.x) {
-            const int o = g * cpg + (int)((i * 4) / T);
-            const float a = inv * (gamma ? gamma[o] : 1.f);
-            const float c = (beta ? beta[o] : 0.f) - mean * a;
-            float4 y = b4[i];
-            y.x = fmaf(y.x, a, c);
-            y.y = fmaf(y.y, a, c);
-            y.z = fmaf(y.z, a, c);
-            y.w = fmaf(y.w, a, c);
-            b4[i] = y;
-        }
-    } else {
-        for (size_t i = threadIdx.x; i < cnt; i += blockDim.x) {
-            const int o = g * cpg + (int)(i / T);
-            const float a = inv * (gamma ? gamma[o] : 1.f);
-            const float c = (beta ? beta[o] : 0.f) - mean * a;
-            base[i] = fmaf(base[i], a, c);
+    // channel by channel: scale and shift are uniform along a channel's T values
+    for (int c = 0; c < cpg; ++c) {
+        const int o = g * cpg + c;
+        const float a = inv * (gamma ? gamma[o] : 1.f);
+        const float sh = (beta ? beta[o] : 0.f) - mean * a;
+        float* row = base + (size_t)c * T;
+        if ((T & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+            float4* r4 = reinterpret_cast<float4*>(row);
+            for (int i = threadIdx.x; i < T / 4; i += blockDim.x) {
+                float4 y = r4[i];
+                y.x = fmaf(y.x, a, sh);
+                y.y = fmaf(y.y, a, sh);
+                y.z = fmaf(y.z, a, sh);
+                y.w = fmaf(y.w, a, sh);
+                r4[i] = y;
+            }
+        } else {
+            for (int i = threadIdx.x; i < T; i += blockDim.x) row[i] = fmaf(row[i], a, sh);
         }
     }
 }

@@ -237,29 +237,33 @@ __global__ void bn_finalize_kernel(const float4* __restrict__ partials, int n_bt
 
 __device__ __forceinline__ float swish_f(float u) { return u / (1.0f + expf(-u)); }
 
+// out[b][j] = swish((y - mean_j) * scale_j + shift_j), in place.  Threads of
+// grid x own 4-column groups (their coefficients stay in registers), grid y
+// strides over the rows.  Columns come 4 at a time when OUT % 4 == 0 and out is
+// 16-byte aligned, one at a time otherwise.
 __global__ void normalize_swish_kernel(float* __restrict__ out, const float* __restrict__ colp,
                                        int B, int OUT) {
-    const size_t total = (size_t)B * OUT;
-    if ((OUT & 3) == 0) {
-        float4* o4 = reinterpret_cast<float4*>(out);
-        for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total / 4;
-             i += (size_t)gridDim.x * blockDim.x) {
-            const int j = (int)((i * 4) % OUT);
-            const float4 c = *reinterpret_cast<const float4*>(colp + j);
-            const float4 s = *reinterpret_cast<const float4*>(colp + OUT + j);
-            const float4 h = *reinterpret_cast<const float4*>(colp + 2 * OUT + j);
-            float4 y = o4[i];
+    const int vec = (OUT % 4 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) ? 4 : 1;
+    const int j = (blockIdx.x * blockDim.x + threadIdx.x) * vec;
+    if (j >= OUT) return;
+    if (vec == 4) {
+        const float4 c = *reinterpret_cast<const float4*>(colp + j);
+        const float4 s = *reinterpret_cast<const float4*>(colp + OUT + j);
+        const float4 h = *reinterpret_cast<const float4*>(colp + 2 * OUT + j);
+        for (int b = blockIdx.y; b < B; b += gridDim.y) {
+            float4* o4 = reinterpret_cast<float4*>(out + (size_t)b * OUT + j);
+            float4 y = *o4;
             y.x = swish_f(fmaf(y.x - c.x, s.x, h.x));
             y.y = swish_f(fmaf(y.y - c.y, s.y, h.y));
             y.z = swish_f(fmaf(y.z - c.z, s.z, h.z));
             y.w = swish_f(fmaf(y.w - c.w, s.w, h.w));
-            o4[i] = y;
+            *o4 = y;
         }
     } else {
-        for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
-             i += (size_t)gridDim.x * blockDim.x) {
-            const int j = (int)(i % OUT);
-            out[i] = swish_f(fmaf(out[i] - colp[j], colp[OUT + j], colp[2 * OUT + j]));
+        const float c = colp[j], s = colp[OUT + j], h = colp[2 * OUT + j];
+        for (int b = blockIdx.y; b < B; b += gridDim.y) {
+            float* o = out + (size_t)b * OUT + j;
+            *o = swish_f(fmaf(*o - c, s, h));
         }
     }
 }
@@ -374,8 +378,12 @@ extern "C" nrc_status nrc_linear_bn_swish(
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
     {
         TraceScope ts("normalize_swish", st);
-        normalize_swish_kernel<<<elementwise_grid((size_t)B * out_f / 4 + 1), 256, 0, st>>>(
-            out, colp, B, out_f);
+        // enough CTAs to fill the GPU several times over: 256 threads cover 1024
+        // (or 256) columns, grid y splits the rows
+        const int vec = (out_f % 4 == 0 && aligned(out, 16)) ? 4 : 1;
+        const int gx = ceil_div(ceil_div(out_f, vec), 256);
+        const int gy = std::max(1, std::min(B, device_sm_count() * 8 / std::max(gx, 1)));
+        normalize_swish_kernel<<<dim3(gx, gy), 256, 0, st>>>(out, colp, B, out_f);
     }
     return cuda_status(cudaGetLastError());
 }
