@@ -58,6 +58,7 @@ struct ConvParams {
     float bn_eps;
     const void* bias;       // (Cout) or NULL
     int bias_off;           // float offset of the staged bias in the extra smem
+    int stage_off;          // byte offset of the bf16 epilogue's two chunk buffers (staged bf16)
     const uint8_t* wpack;   // packed weight image
     // group statistics (conv + GroupNorm)
     float2* partials;       // [((n*G + g) * n_tt + tt) * 128 + row] = (mean, M2) of the
@@ -133,6 +134,8 @@ struct ConvProblem {
     static constexpr int kAlign = 16 / (int)sizeof(T);   // box starts on 16-byte boundaries
     static constexpr int kBoxW = kBM + kAlign;            // rows (time positions) per box
     static constexpr uint32_t kBoxBytes = (uint32_t)(kBoxW * kBK * sizeof(T));
+    // Staged bf16 residual epilogue: two chunk buffers of 16 channels x 128 rows.
+    static constexpr uint32_t kChunkBufBytes = 16u * kBM * 2u;
 
     static __device__ __forceinline__ Tile tile_info(const Params& p, int tile) {
         return conv_tile(p, tile);
@@ -279,9 +282,83 @@ struct ConvProblem {
             // otherwise idle during the mainloop), later chunks four ahead of
             // the drain.  Path tests are uniform per chunk (t_ok per lane), so
             // a full chunk drains as straight-line code.
+            const int ovalid = p.Cout - obase;     // channels of this tile that exist
+            if constexpr (STAGED && sizeof(T) == 2) {
+                // bf16 rows 16-byte aligned: a warp owns only 32 rows (half a
+                // 128-byte line of one channel), so the four epilogue warps
+                // move each 16-channel chunk through a shared buffer and touch
+                // global memory in full lines: warp q loads/stores channel rows
+                // 4q .. 4q+3 of the chunk, lane l rows 4l .. 4l+3 (8 bytes).
+                // Named barrier 1 orders the four warps; whether the tile's
+                // accumulator is ready is decided for all four at once (the
+                // AND of their waits), so they always meet the same barriers.
+                const int t0 = tl.tt * kBM;
+                const bool rows_ok = t0 + 4 * lane < p.L;       // L % 8 == 0: all 4 or none
+                const size_t grow = (row0 + obase + 4 * quarter) * p.L + (size_t)(t0 + 4 * lane);
+                const uint2* xq = reinterpret_cast<const uint2*>(static_cast<const T*>(p.x) + grow);
+                uint2* oq = reinterpret_cast<uint2*>(out + grow);
+                const size_t rstride = (size_t)p.L / 4;          // one channel row, in uint2
+                const uint32_t buf0 = smem_u32(extra + p.stage_off);
+                const uint32_t mine = (uint32_t)(32 * quarter + lane) * 2u;   // this lane's row
+                const uint32_t coop = (uint32_t)(4 * quarter * kBM + 4 * lane) * 2u;
+                auto fetch = [&](int cc, uint2 (&w)[4]) {
+                    if (cc >= BN) return;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        w[r] = (rows_ok && cc + 4 * quarter + r < ovalid)
+                                   ? __ldg(xq + (size_t)(cc + r) * rstride)
+                                   : make_uint2(0u, 0u);
+                };
+                uint32_t bsel = 0;
+                auto emit = [&](int cc, uint2 (&w)[4]) {
+                    const uint32_t buf = buf0 + bsel * kChunkBufBytes;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        st_shared_v2(buf + coop + (uint32_t)(r * kBM * 2), w[r].x, w[r].y);
+                    fetch(cc + 64, w);          // refill this buffer four chunks ahead
+                    named_bar_sync(1, 128);     // the chunk's residual is staged
+                    float v[16];
+                    tmem_ld16(taddr + (uint32_t)cc, v);
+                    const float4* b4 = reinterpret_cast<const float4*>(bias_s + cc);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 bq = b4[q];
+                        v[4 * q] += bq.x;
+                        v[4 * q + 1] += bq.y;
+                        v[4 * q + 2] += bq.z;
+                        v[4 * q + 3] += bq.w;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t a = buf + mine + (uint32_t)(i * kBM * 2);
+                        const float y = v[i] + ld_shared_bf16(a);
+                        st_shared_u16(a, __bfloat16_as_ushort(__float2bfloat16_rn(y)));
+                    }
+                    named_bar_sync(1, 128);     // the chunk's output is staged
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const uint2 o = ld_shared_v2(buf + coop + (uint32_t)(r * kBM * 2));
+                        if (rows_ok && cc + 4 * quarter + r < ovalid)
+                            oq[(size_t)(cc + r) * rstride] = o;
+                    }
+                    bsel ^= 1u;
+                };
+                uint2 w0[4], w1[4], w2[4], w3[4];
+                fetch(0, w0);
+                fetch(16, w1);
+                fetch(32, w2);
+                fetch(48, w3);
+                if (!named_bar_and(1, 128, acquire())) return false;
+                for (int cc = 0; cc < BN; cc += 64) {
+                    emit(cc, w0);
+                    if (cc + 16 < BN) emit(cc + 16, w1);
+                    if (cc + 32 < BN) emit(cc + 32, w2);
+                    if (cc + 48 < BN) emit(cc + 48, w3);
+                }
+                return true;
+            }
             const T* xr = static_cast<const T*>(p.x) + (row0 + obase) * p.L + t;
             T* outr = out + (row0 + obase) * p.L + t;
-            const int ovalid = p.Cout - obase;     // channels of this tile that exist
             auto fetch = [&](int cc, float (&r)[16]) {
                 if (cc >= BN) return;
                 const T* xp = xr + (size_t)cc * p.L;
@@ -570,19 +647,24 @@ __global__ void groupnorm_finalize_normalize_kernel(float* __restrict__ out,
 struct ConvPlan {
     GemmPlan g;
     int n_ot, n_chunks, n_tt;
+    int stage_off;          // byte offset of the epilogue's chunk buffers in the extra smem
     size_t wpack_bytes;
 };
 
+// Extra shared memory: BN fold (scale, shift) when present, the staged bias,
+// then (128-byte aligned) stage_bytes for the epilogue's chunk buffers.
 static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn,
-                          uint32_t x_box_bytes = 0) {
+                          uint32_t x_box_bytes = 0, uint32_t stage_bytes = 0) {
     ConvPlan pl{};
     const int BN = Cout <= 256 ? ((Cout + 15) / 16) * 16 : 256;
     pl.n_ot = ceil_div(Cout, BN);
     pl.n_chunks = ceil_div(Cin, kBK);
     pl.n_tt = ceil_div(L, kBM);
     const long long tiles = (long long)N * pl.n_tt * pl.n_ot;
-    const uint32_t extra = (with_bn ? (uint32_t)(2 * pl.n_chunks * kBK * 4) : 0u) +
-                           (uint32_t)((pl.n_ot * BN + 32) * 4);
+    const uint32_t fold_bias = (with_bn ? (uint32_t)(2 * pl.n_chunks * kBK * 4) : 0u) +
+                               (uint32_t)((pl.n_ot * BN + 32) * 4);
+    pl.stage_off = (int)((fold_bias + 127u) & ~127u);
+    const uint32_t extra = stage_bytes ? (uint32_t)pl.stage_off + stage_bytes : fold_bias;
     pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), 3 * pl.n_chunks, NP,
                           extra, x_box_bytes);
     pl.wpack_bytes = (size_t)pl.n_ot * pl.g.num_kiters * NP * BN * 128;
@@ -611,9 +693,16 @@ static bool plan_conv_staged(ConvParams& p, ConvPlan& pl, int N, int Cin, int Co
                              bool with_bn) {
     constexpr int NP = sizeof(T) == 4 ? 2 : 1;
     constexpr uint32_t box_bytes = (uint32_t)((kBM + 16 / sizeof(T)) * kBK * sizeof(T));
+    // the staged bf16 residual epilogue needs its two chunk buffers
+    const uint32_t stage_bytes =
+        (with_bn && sizeof(T) == 2) ? 2u * ConvProblem<T, ConvEpi::kResidual, true>::kChunkBufBytes
+                                    : 0u;
     if (make_x_map<T>(p, p.x, N, Cin, L, with_bn)) {
-        pl = plan_conv(N, Cin, Cout, L, NP, with_bn, box_bytes);
-        if (pl.g.b_stages >= 2 && pl.g.x_depth >= 2) return true;
+        pl = plan_conv(N, Cin, Cout, L, NP, with_bn, box_bytes, stage_bytes);
+        if (pl.g.b_stages >= 2 && pl.g.x_depth >= 2) {
+            p.stage_off = pl.stage_off;
+            return true;
+        }
     }
     pl = plan_conv(N, Cin, Cout, L, NP, with_bn);
     return false;
