@@ -225,6 +225,13 @@ def barrier(world):
         dist.barrier()
 
 
+def whole_job_tflops(world, flops_per_rank_step, ms_per_step):
+    """Weak scaling: every rank processes its own copy of the workload each step,
+    so the job's throughput is world x the per-rank work over the slowest rank's
+    step time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def max_over_ranks(world, value, device=None):
     if world <= 1:
         return value
@@ -367,7 +374,7 @@ def gpu_arm(args, world, rank, local):
     main_ms = statistics.mean(per_kernel[main])
 
     ms_per_step = total_ms / steps
-    value = world * info["flops"] / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, info["flops"], ms_per_step)
     peaks, peaks_src = load_peaks()
     tensor_peak, tensor_note = roofline_peaks(info, peaks)
     hbm_peak = peaks["hbm_gbs"]
