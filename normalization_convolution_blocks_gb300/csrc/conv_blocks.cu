@@ -266,10 +266,11 @@ struct ConvProblem {
         return p.wpack + ((size_t)tl.ot * p.n_kiters + kiter) * NP * (size_t)p.BN * 128u;
     }
 
-    template <class Acquire>
+    template <class Acquire, class Release>
     static __device__ __forceinline__ bool epilogue(const Params& p, const uint8_t* extra,
                                                     const Tile& tl, int quarter, int lane,
-                                                    uint32_t taddr, int BN, Acquire& acquire) {
+                                                    uint32_t taddr, int BN, int halves,
+                                                    Acquire& acquire, Release& release) {
         const int t = tl.tt * kBM + quarter * 32 + lane;
         const bool t_ok = t < p.L;
         T* out = static_cast<T*>(p.out);
@@ -348,13 +349,18 @@ struct ConvProblem {
                 fetch(16, w1);
                 fetch(32, w2);
                 fetch(48, w3);
-                if (!named_bar_and(1, 128, acquire())) return false;
+                if (!named_bar_and(1, 128, acquire(0))) return false;
                 for (int cc = 0; cc < BN; cc += 64) {
+                    if (halves == 2 && cc == BN / 2) {   // half A read: hand it back
+                        release(0);
+                        if (!named_bar_and(1, 128, acquire(1))) return false;
+                    }
                     emit(cc, w0);
                     if (cc + 16 < BN) emit(cc + 16, w1);
                     if (cc + 32 < BN) emit(cc + 32, w2);
                     if (cc + 48 < BN) emit(cc + 48, w3);
                 }
+                release(halves - 1);
                 return true;
             }
             const T* xr = static_cast<const T*>(p.x) + (row0 + obase) * p.L + t;
@@ -403,13 +409,18 @@ struct ConvProblem {
             fetch(16, r1);
             fetch(32, r2);
             fetch(48, r3);
-            if (!acquire()) return false;
+            if (!acquire(0)) return false;
             for (int cc = 0; cc < BN; cc += 64) {
+                if (halves == 2 && cc == BN / 2) {   // half A read: hand it back
+                    release(0);
+                    if (!acquire(1)) return false;
+                }
                 emit(cc, r0);
                 if (cc + 16 < BN) emit(cc + 16, r1);
                 if (cc + 32 < BN) emit(cc + 32, r2);
                 if (cc + 48 < BN) emit(cc + 48, r3);
             }
+            release(halves - 1);
         } else {
             // y -> out, and per-(n, group, t tile, row) statistics of y.  A
             // group's channels are contiguous.  Each run of a group inside a
@@ -417,7 +428,8 @@ struct ConvProblem {
             // M2), folded into the group's running triple with Chan's update,
             // and merged across the warp when the group ends.  Every test below
             // is uniform across the warp except t_ok (invalid rows count 0).
-            if (!acquire()) return false;
+            for (int h = 0; h < halves; ++h)
+                if (!acquire(h)) return false;
             const int ovalid = p.Cout - obase;
             float cnt = 0.f, mean = 0.f, m2 = 0.f;
             const float tw = t_ok ? 1.f : 0.f;
@@ -511,6 +523,7 @@ struct ConvProblem {
                     i0 = i1;
                 }
             }
+            for (int h = 0; h < halves; ++h) release(h);
         }
         return true;
     }
@@ -763,6 +776,11 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual(
     p.bias = conv_bias;
     p.bias_off = 2 * pl.n_chunks * kBK;
     p.wpack = static_cast<const uint8_t*>(workspace);
+    // Residual drain overlapped at tile boundaries (whole 128-column halves).
+    if (pl.g.BN % 128 == 0) {
+        const int SA = 256 / (32 * NP);
+        pl.g.split_h = std::min(std::min(SA, pl.g.b_stages), pl.g.num_kiters / 2);
+    }
     const size_t units = pl.wpack_bytes / 16 / NP;
     if (dt == NRC_F32) {
         {

@@ -112,11 +112,13 @@ struct LinearProblem {
         return p.xpack + ((size_t)tl.bt * p.n_kiters + kiter) * 2 * (size_t)p.BN * 128u;
     }
 
-    template <class Acquire>
+    template <class Acquire, class Release>
     static __device__ __forceinline__ bool epilogue(const Params& p, const uint8_t*,
                                                     const Tile& tl, int quarter, int lane,
-                                                    uint32_t taddr, int BN, Acquire& acquire) {
-        if (!acquire()) return false;
+                                                    uint32_t taddr, int BN, int halves,
+                                                    Acquire& acquire, Release& release) {
+        for (int h = 0; h < halves; ++h)
+            if (!acquire(h)) return false;
         const int j = tl.jt * kBM + quarter * 32 + lane;
         const bool j_ok = j < p.OUT;
         const float lb = (j_ok && p.lin_bias) ? __ldg(p.lin_bias + j) : 0.f;
@@ -152,6 +154,7 @@ struct LinearProblem {
             }
         }
         if (j_ok) p.partials[(size_t)tl.bt * p.OUT + j] = make_float4(cnt, mean, m2, 0.f);
+        for (int h = 0; h < halves; ++h) release(h);
         return true;
     }
 };

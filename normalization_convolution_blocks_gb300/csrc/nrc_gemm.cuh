@@ -13,7 +13,12 @@
 //   * B (the weight side) is bulk-copied (cp.async.bulk) from a pre-packed
 //     global image into a ring of shared-memory stages in the 128-byte swizzle
 //     layout the MMA's shared-memory descriptor expects.
-//   * The fp32 accumulator lives in TMEM; the epilogue warps drain it.
+//   * The fp32 accumulator lives in TMEM; the epilogue warps drain it.  With
+//     cfg.split_h = H > 0 the accumulator's two column halves are handed over
+//     separately at tile boundaries: the MMAs finish half A over the tile's
+//     last H stages (all resident) before half B, so the epilogue starts on
+//     half A while half B is still being computed; and the next tile's first
+//     H stages run on half A as soon as it is drained, before half B is.
 //
 // Keeping A out of shared memory leaves shared-memory bandwidth to the weight
 // stream alone, which the MMAs read at 64 B/clk at full rate.
@@ -66,6 +71,8 @@ struct GemmCfg {
     uint32_t b_stage_bytes; // NP * BN * 128
     int x_depth;            // A-source ring slots (0: A loaded to registers)
     uint32_t x_box_bytes;   // bytes of one slot: one stage's box (a multiple of 128)
+    int split_h;            // >0: hand the accumulator over in column halves, H stages at
+                            // each tile end (H <= both ring depths, 2H <= num_kiters)
     int* status;            // device status word
     unsigned long long timeout_ns;
 };
@@ -113,14 +120,16 @@ __device__ __forceinline__ void split_store_a(uint32_t taddr_hi, const float (&v
 //        -> A[row][kiter*64 + k0 .. +32) from the landed slot, transform applied
 //   static __device__ const void* b_src(const Params&, const Tile&, int kiter)
 //        -> packed B image of the stage: NP parts of BN rows x 128 B, swizzled
-//   template <class Acquire>
+//   template <class Acquire, class Release>
 //   static __device__ bool epilogue(const Params&, const uint8_t* extra, const Tile&,
 //                                   int quarter, int lane, uint32_t taddr, int BN,
-//                                   Acquire& acquire)
-//        -> may issue loads that do not need the accumulator, then calls acquire()
-//           (waits for the tile's accumulator; false = pipeline aborted, return
-//           false), then drains TMEM columns [taddr, taddr + BN) of its lane
-//           quarter (every lane executes the tcgen05.ld calls)
+//                                   int halves, Acquire& acquire, Release& release)
+//        -> may issue loads that do not need the accumulator, then for each of the
+//           `halves` column halves (1: the whole tile; 2: [0, BN/2) then
+//           [BN/2, BN)) calls acquire(h) before reading it (false = pipeline
+//           aborted, return false) and release(h) once it has read it; drains
+//           TMEM columns [taddr, taddr + BN) of its lane quarter (every lane
+//           executes the tcgen05.ld calls)
 template <class Prob, int NP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ typename Prob::Params p, const GemmCfg cfg) {
@@ -143,9 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto a_empty = [&](int s) { return bar0 + 8u * (uint32_t)(kMaxStages + s); };
     auto b_full = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kMaxStages + s); };
     auto b_empty = [&](int s) { return bar0 + 8u * (uint32_t)(3 * kMaxStages + s); };
-    const uint32_t acc_full = bar0 + 8u * (uint32_t)(4 * kMaxStages);
-    const uint32_t acc_empty = acc_full + 8u;
-    const uint32_t drain_bar = acc_full + 16u;
+    // Accumulator column half h: full (MMA commit) / empty (epilogue warps).
+    const uint32_t drain_bar = bar0 + 8u * (uint32_t)(4 * kMaxStages);
+    auto acc_full = [&](int h) { return drain_bar + 8u + 16u * (uint32_t)h; };
+    auto acc_empty = [&](int h) { return drain_bar + 16u + 16u * (uint32_t)h; };
     // A-source slot j: full (TMA complete_tx) / empty (producer warps)
     auto x_full = [&](int j) { return bar0 + 8u * (uint32_t)(4 * kMaxStages + 5 + j); };
     auto x_empty = [&](int j) {
@@ -165,8 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_full(s), 1);      // producer's arrive.expect_tx
             mbar_init(b_empty(s), 1);     // MMA commit
         }
-        mbar_init(acc_full, 1);           // MMA commit
-        mbar_init(acc_empty, 4);          // one arrival per epilogue warp
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(acc_full(h), 1);    // MMA commit
+            mbar_init(acc_empty(h), 4);   // one arrival per epilogue warp
+        }
         mbar_init(drain_bar, 1);
         for (int j = 0; j < cfg.x_depth; ++j) {
             mbar_init(x_full(j), 1);                  // the issuer's arrive.expect_tx
@@ -218,45 +230,130 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kBM, BN);
+            const int H = cfg.split_h;
+            const int HB = BN / 2;                      // columns of a half
+            const uint32_t idesc_full = idesc_bf16_f32(kBM, BN);
+            const uint32_t idesc_half = idesc_bf16_f32(kBM, HB);
             int sa = 0, sb = 0;
             uint32_t pha = 0, phb = 0;
             bool ok = true;
             int it = 0;
-            for (int tile = blockIdx.x; ok && tile < cfg.num_tiles; tile += gridDim.x, ++it) {
-                if (!mbar_wait(acc_empty, ((uint32_t)it & 1u) ^ 1u, ctx, kSiteAccEmpty)) {
-                    ok = false;
-                    break;
-                }
+            // Ring slot and phase i stages past the cursor (i < ring depth).
+            auto a_at = [&](int i, int& s, uint32_t& ph) {
+                s = sa + i;
+                ph = pha;
+                if (s >= SA) { s -= SA; ph ^= 1u; }
+            };
+            auto b_at = [&](int i, int& s, uint32_t& ph) {
+                s = sb + i;
+                ph = phb;
+                if (s >= SB) { s -= SB; ph ^= 1u; }
+            };
+            auto wait_stage = [&](int i) -> bool {
+                int s;
+                uint32_t ph;
+                a_at(i, s, ph);
+                if (!mbar_wait(a_full(s), ph, ctx, kSiteFullA)) return false;
+                b_at(i, s, ph);
+                if (!mbar_wait(b_full(s), ph, ctx, kSiteFullB)) return false;
                 tc_fence_after();
-                for (int k = 0; k < cfg.num_kiters; ++k) {
-                    if (!mbar_wait(a_full(sa), pha, ctx, kSiteFullA) ||
-                        !mbar_wait(b_full(sb), phb, ctx, kSiteFullB)) {
+                return true;
+            };
+            // MMAs of the stage i past the cursors into columns [c0, c0 + n) (B
+            // rows c0 ..); `first` starts that column range afresh.
+            auto mma_stage = [&](int i, int c0, uint32_t idesc, bool first) {
+                int s_a, s_b;
+                uint32_t ph;
+                a_at(i, s_a, ph);
+                b_at(i, s_b, ph);
+                const uint32_t a_col = tmem_base + kTmemARing + (uint32_t)(s_a * 32 * NP);
+                const uint32_t b_hi =
+                    smem_u32(smem + (size_t)s_b * cfg.b_stage_bytes) + (uint32_t)c0 * 128u;
+                const uint32_t d = tmem_base + (uint32_t)c0;
+#pragma unroll
+                for (int kk = 0; kk < kBK / kUMMA_K; ++kk) {
+                    const uint32_t a_k = a_col + (uint32_t)(kk * kUMMA_K / 2);
+                    const uint64_t bd = sw128_kmajor_desc(b_hi + (uint32_t)kk * (kUMMA_K * 2));
+                    mma_bf16_ts(d, a_k, bd, idesc, (first && kk == 0) ? 0u : 1u);
+                    if constexpr (NP == 2) {
+                        const uint64_t bd_lo = sw128_kmajor_desc(
+                            b_hi + (uint32_t)BN * 128u + (uint32_t)kk * (kUMMA_K * 2));
+                        mma_bf16_ts(d, a_k + 32u, bd, idesc, 1u);   // lo * hi
+                        mma_bf16_ts(d, a_k, bd_lo, idesc, 1u);      // hi * lo
+                    }
+                }
+            };
+            // Frees the stage at the cursors once its MMAs finish; advances.
+            auto retire = [&]() {
+                mma_commit(a_empty(sa));
+                mma_commit(b_empty(sb));
+                if (++sa == SA) { sa = 0; pha ^= 1u; }
+                if (++sb == SB) { sb = 0; phb ^= 1u; }
+            };
+            for (int tile = blockIdx.x; ok && tile < cfg.num_tiles; tile += gridDim.x, ++it) {
+                const uint32_t epar = ((uint32_t)it & 1u) ^ 1u;   // previous use drained
+                if (H == 0) {
+                    if (!mbar_wait(acc_empty(0), epar, ctx, kSiteAccEmpty)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_col = tmem_base + kTmemARing + (uint32_t)(sa * 32 * NP);
-                    const uint32_t b_hi = smem_u32(smem + (size_t)sb * cfg.b_stage_bytes);
-#pragma unroll
-                    for (int kk = 0; kk < kBK / kUMMA_K; ++kk) {
-                        const uint32_t a_k = a_col + (uint32_t)(kk * kUMMA_K / 2);
-                        const uint64_t bd = sw128_kmajor_desc(b_hi + (uint32_t)kk * (kUMMA_K * 2));
-                        mma_bf16_ts(tmem_base, a_k, bd, idesc, (k | kk) != 0 ? 1u : 0u);
-                        if constexpr (NP == 2) {
-                            const uint64_t bd_lo = sw128_kmajor_desc(
-                                b_hi + (uint32_t)BN * 128u + (uint32_t)kk * (kUMMA_K * 2));
-                            mma_bf16_ts(tmem_base, a_k + 32u, bd, idesc, 1u);   // lo * hi
-                            mma_bf16_ts(tmem_base, a_k, bd_lo, idesc, 1u);      // hi * lo
+                    for (int k = 0; k < cfg.num_kiters; ++k) {
+                        if (!wait_stage(0)) {
+                            ok = false;
+                            break;
                         }
+                        mma_stage(0, 0, idesc_full, k == 0);
+                        retire();
                     }
-                    mma_commit(a_empty(sa));           // A stage free once these finish
-                    mma_commit(b_empty(sb));           // B stage likewise
-                    if (++sa == SA) { sa = 0; pha ^= 1u; }
-                    if (++sb == SB) { sb = 0; phb ^= 1u; }
+                    if (!ok) break;
+                    mma_commit(acc_full(0));           // accumulator ready for the epilogue
+                    continue;
+                }
+                // head: the first H stages on half A as soon as it is drained,
+                // then on half B
+                if (!mbar_wait(acc_empty(0), epar, ctx, kSiteAccEmpty)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int i = 0; i < H && ok; ++i) {
+                    ok = wait_stage(i);
+                    if (ok) mma_stage(i, 0, idesc_half, i == 0);
                 }
                 if (!ok) break;
-                mma_commit(acc_full);                  // accumulator ready for the epilogue
+                if (!mbar_wait(acc_empty(1), epar, ctx, kSiteAccEmpty)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int i = 0; i < H; ++i) {
+                    mma_stage(0, HB, idesc_half, i == 0);
+                    retire();
+                }
+                // body: full width
+                for (int k = H; k < cfg.num_kiters - H; ++k) {
+                    if (!wait_stage(0)) {
+                        ok = false;
+                        break;
+                    }
+                    mma_stage(0, 0, idesc_full, false);
+                    retire();
+                }
+                if (!ok) break;
+                // tail: the last H stages on half A, which is then complete,
+                // then on half B
+                for (int i = 0; i < H && ok; ++i) {
+                    ok = wait_stage(i);
+                    if (ok) mma_stage(i, 0, idesc_half, false);
+                }
+                if (!ok) break;
+                mma_commit(acc_full(0));
+                for (int i = 0; i < H; ++i) {
+                    mma_stage(0, HB, idesc_half, false);
+                    retire();
+                }
+                mma_commit(acc_full(1));
             }
             if (!ok) {
                 // Every MMA issued so far must finish before TMEM/smem go away.
@@ -394,21 +491,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         for (int tile = blockIdx.x; tile < cfg.num_tiles; tile += gridDim.x, ++it) {
             const Tile tl = Prob::tile_info(p, tile);
-            // The block's epilogue calls acquire() once it has issued whatever
-            // it can load before the accumulator is ready.
-            auto acquire = [&]() -> bool {
+            // The block's epilogue calls acquire(h) once it has issued whatever
+            // it can load before column half h is ready, release(h) once it
+            // has read it.
+            auto acquire = [&](int h) -> bool {
                 int w_ok = 1;
-                if (lane == 0) w_ok = mbar_wait(acc_full, (uint32_t)it & 1u, ctx, kSiteAccFull);
+                if (lane == 0)
+                    w_ok = mbar_wait(acc_full(h), (uint32_t)it & 1u, ctx, kSiteAccFull);
                 w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
                 if (w_ok) tc_fence_after();
                 return w_ok != 0;
             };
+            auto release = [&](int h) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty(h));
+            };
             if (!Prob::epilogue(p, extra, tl, quarter, lane,
-                                tmem_base + ((uint32_t)(quarter * 32) << 16), BN, acquire))
+                                tmem_base + ((uint32_t)(quarter * 32) << 16), BN,
+                                cfg.split_h > 0 ? 2 : 1, acquire, release))
                 break;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
         }
     }
 

@@ -12,6 +12,7 @@ namespace nrc {
 
 struct GemmPlan {
     int BN, num_tiles, num_kiters, b_stages, x_depth;
+    int split_h;            // accumulator handed over in column halves, H stages (0: whole)
     uint32_t b_stage_bytes, x_box_bytes, extra_bytes, smem_bytes;
 };
 
@@ -72,6 +73,13 @@ inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
     cfg.b_stage_bytes = pl.b_stage_bytes;
     cfg.x_depth = pl.x_depth;
     cfg.x_box_bytes = pl.x_box_bytes;
+    cfg.split_h = pl.split_h;
+    {   // the halves need both rings to hold H stages at once, and whole halves
+        constexpr int SA = (int)((kTmemCols - kTmemARing) / (32u * NP));
+        if (pl.split_h < 0 || pl.split_h > SA || pl.split_h > pl.b_stages ||
+            2 * pl.split_h > pl.num_kiters || (pl.split_h > 0 && pl.BN % 128 != 0))
+            return NRC_ERR_UNSUPPORTED;
+    }
     cfg.status = device_status_ptr();
     cfg.timeout_ns = wait_timeout_ns();
     if (cfg.status == nullptr) return NRC_ERR_CUDA;
