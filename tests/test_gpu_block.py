@@ -51,6 +51,26 @@ def test_shapes_fp32(N, C, L, d):
     assert_f32(_gpu(dev, inp), _oracle(inp), f"N{N} C{C} L{L} d{d}")
 
 
+@pytest.mark.parametrize("N,C,L,d", [
+    (2, 128, 256, 4),       # 6 K stages: the column-half hand-over has no body stages
+    (1, 2048, 64, 1),       # largest supported C: 96 K stages, 8 output tiles
+])
+def test_edge_shapes_fp32(N, C, L, d):
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(N, C, L, d, seed=N * 7 + C + d)
+    assert_f32(_gpu(dev, inp), _oracle(inp), f"N{N} C{C} L{L} d{d}")
+
+
+@pytest.mark.parametrize("N,C,L,d", [
+    (1, 128, 264, 2),       # 6 K stages, ragged tail
+    (1, 768, 136, 3),       # three output tiles
+])
+def test_edge_shapes_bf16(N, C, L, d):
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(N, C, L, d, seed=N * 11 + C + d, dtype=torch.bfloat16)
+    assert_bf16(_gpu(dev, inp), _oracle(inp), f"bf16 N{N} C{C} L{L} d{d}")
+
+
 def test_no_bias():
     dev = need_gpu()
     inp = syn.prenorm_block_inputs(2, 64, 256, 16, seed=5)
