@@ -47,11 +47,11 @@ L2_FLUSH_BYTES = 256 << 20
 # one ncu capture (profiles/), keyed by workload; valid only while the kernel
 # sources hash to the recorded value.
 NCU_TRAFFIC = {
-    "prenorm_block_f32": {"bytes": 221881088, "src_hash": "af2731dddfe61809",
+    "prenorm_block_f32": {"bytes": 221731072, "src_hash": "137fb19427aaca81",
                           "profile": "profiles/gemm_prenorm_block_f32_N32_C256_L4096_d128.md"},
-    "linear_bn_swish_f32": {"bytes": 359364352, "src_hash": "af2731dddfe61809",
+    "linear_bn_swish_f32": {"bytes": 359206144, "src_hash": "137fb19427aaca81",
                             "profile": "profiles/gemm_linear_bn_swish_f32_B1024_IN8192_OUT8192.md"},
-    "conv1d_groupnorm_f32": {"bytes": 8828160, "src_hash": "af2731dddfe61809",
+    "conv1d_groupnorm_f32": {"bytes": 8852736, "src_hash": "137fb19427aaca81",
                              "profile": "profiles/gemm_conv1d_groupnorm_f32_N16_C128_256_T1024_G32.md"},
 }
 
