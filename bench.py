@@ -263,10 +263,13 @@ def make_call(name, dev, host=False):
     if wl.kind == "block":
         x, rm, rv, g, b, w, bias = map(place, (inp.x, inp.running_mean, inp.running_var,
                                               inp.gamma, inp.beta, inp.weight, inp.bias))
-        out = None if host else torch.empty_like(x)
-        ws = None if host else torch.empty(
-            api.prenorm_dilconv_residual_workspace_size(x.shape[1], x.dtype), dtype=torch.uint8,
-            device=dev)
+        # host buffers: the output is pinned and the workspace allocated once, as
+        # a caller running the block repeatedly would hold them
+        out = torch.empty(x.shape, dtype=x.dtype, pin_memory=True) if host else \
+            torch.empty_like(x)
+        ws_bytes = api.prenorm_dilconv_residual_host_workspace_size(*x.shape, x.dtype) if host \
+            else api.prenorm_dilconv_residual_workspace_size(x.shape[1], x.dtype)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         tensors_in = (x, rm, rv, g, b, w, bias)
 
         def call():

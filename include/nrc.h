@@ -96,6 +96,39 @@ nrc_status nrc_prenorm_dilconv_residual(
     void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Pre-norm residual block on HOST buffers.  Same computation and errors as
+ * nrc_prenorm_dilconv_residual ("Kimi-K2.6 l2_p12", problem statement), for
+ * callers whose x and out live in host memory.
+ *
+ * x_host, out_host: (N, C, L) in host memory, dtype `dt`; page-locked
+ *   (cudaHostAlloc / pinned) memory lets the copies overlap the GPU work,
+ *   pageable memory still works but serialises.
+ * bn_*_host, weight_host, bias_host: as in nrc_prenorm_dilconv_residual but in
+ *   host memory (bias_host may be NULL).
+ * chunk_n: samples per pipeline chunk (>= 1; clamped to N).  The batch flows
+ *   through two device buffers: the copy-in of chunk j+1, the GEMM of chunk j
+ *   and the copy-out of chunk j-1 run at once, on two library-owned streams
+ *   (created once per device) and `stream`, ordered by events.
+ * workspace: DEVICE memory, 256-byte aligned, of at least
+ *   nrc_prenorm_dilconv_residual_host_workspace_size(N, C, L, dt, chunk_n)
+ *   bytes (weight image, parameters, two x and two out chunk buffers).
+ * Asynchronous: work already on `stream` comes first; `stream` resumes after
+ * the last copy-out, so synchronising `stream` makes out_host valid.  Calls
+ * from several host threads are serialised inside the library (they share the
+ * per-device streams); host buffers must stay valid until then.
+ * ------------------------------------------------------------------------ */
+size_t nrc_prenorm_dilconv_residual_host_workspace_size(int N, int C, int L, nrc_dtype dt,
+                                                        int chunk_n);
+
+nrc_status nrc_prenorm_dilconv_residual_host(
+    const void *x_host, void *out_host, nrc_dtype dt, int N, int C, int L,
+    int kernel_size, int dilation, int padding,
+    const float *bn_running_mean_host, const float *bn_running_var_host,
+    const float *bn_gamma_host, const float *bn_beta_host, float bn_eps,
+    const void *conv_weight_host, const void *conv_bias_host, int chunk_n,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Allocation-free pre-norm residual block.  The pages have no counterpart:
  * this is a library convenience, not part of the method.
  *

@@ -6,9 +6,11 @@ allocated with torch.  Every step of every block runs in the library's CUDA
 kernels; there is no CPU fallback -- if the library is not built, or no GPU
 is present, the calls raise.
 
-Host (CPU) input tensors are accepted for end-to-end use: they are copied to
-the current device before the call (non-blocking when pinned) and the result
-is copied back to host memory.
+Host (CPU) input tensors are accepted for end-to-end use.  The pre-norm block
+hands them to the library's host-buffer entry point, which pipelines the copies
+with the GPU work (pinned memory lets them overlap); the other blocks copy them
+to the current device before the call.  The result comes back in host memory,
+ready when the call returns.
 """
 from __future__ import annotations
 
@@ -53,6 +55,9 @@ def load() -> ctypes.CDLL:
         "nrc_prenorm_dilconv_residual_workspace_size": ([i, i], sz),
         "nrc_prenorm_dilconv_residual": ([p, p, i, i, i, i, i, i, i, p, p, p, p, f, p, p, p, sz,
                                           p], i),
+        "nrc_prenorm_dilconv_residual_host_workspace_size": ([i, i, i, i, i], sz),
+        "nrc_prenorm_dilconv_residual_host": ([p, p, i, i, i, i, i, i, i, p, p, p, p, f, p, p, i,
+                                               p, sz, p], i),
         "nrc_prenorm_dilconv_residual_noalloc_max_bytes": ([], sz),
         "nrc_prenorm_dilconv_residual_noalloc": ([p, p, i, i, i, i, i, i, i, p, p, p, p, f, p, p,
                                                   p], i),
@@ -129,17 +134,22 @@ def prenorm_dilconv_residual_workspace_size(C: int, dtype=torch.float32) -> int:
 
 def prenorm_dilconv_residual(x, bn_running_mean, bn_running_var, bn_gamma, bn_beta, bn_eps,
                              conv_weight, conv_bias, dilation, padding=None, kernel_size=3,
-                             out=None, workspace=None, stream=None):
+                             out=None, workspace=None, stream=None, chunk_n=None):
     """out = x + Conv1d(ReLU(BatchNorm1d_eval(x))) with k=3, padding=dilation.
 
     x (N, C, L) fp32 or bf16; BN tensors (C) fp32; conv_weight (C, C, 3) and
-    conv_bias (C) in x's dtype (bias may be None)."""
+    conv_bias (C) in x's dtype (bias may be None).  With x in host memory the
+    result is a host tensor, computed in chunks of chunk_n samples (default
+    N/8) whose copies overlap the GPU work."""
     lib = load()
-    host = not x.is_cuda
     dev = _target_device(x)
     if x.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("x must be float32 or bfloat16")
     dt = NRC_F32 if x.dtype == torch.float32 else NRC_BF16
+    if not x.is_cuda:
+        return _prenorm_host(lib, dev, dt, x, bn_running_mean, bn_running_var, bn_gamma,
+                             bn_beta, bn_eps, conv_weight, conv_bias, dilation, padding,
+                             kernel_size, out, workspace, stream, chunk_n)
     xd = _dev(x, dev)
     N, C, L = xd.shape
     rm, rv, g, b = (_dev(t, dev, torch.float32) for t in (bn_running_mean, bn_running_var,
@@ -147,7 +157,7 @@ def prenorm_dilconv_residual(x, bn_running_mean, bn_running_var, bn_gamma, bn_be
     w = _dev(conv_weight, dev, x.dtype)
     cb = _dev(conv_bias, dev, x.dtype)
     padding = dilation if padding is None else padding
-    o = out if (out is not None and not host) else torch.empty_like(xd)
+    o = out if out is not None else torch.empty_like(xd)
     need = lib.nrc_prenorm_dilconv_residual_workspace_size(C, dt)
     ws = _workspace(need, dev, workspace)
     st = lib.nrc_prenorm_dilconv_residual(
@@ -156,11 +166,50 @@ def prenorm_dilconv_residual(x, bn_running_mean, bn_running_var, bn_gamma, bn_be
         _stream(stream))
     _check(st, "nrc_prenorm_dilconv_residual")
     _keep_alive(stream, xd, rm, rv, g, b, w, cb, ws)
-    if host:
-        res = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        res.copy_(o, non_blocking=False)
-        return res
     return o
+
+
+def prenorm_dilconv_residual_host_workspace_size(N, C, L, dtype=torch.float32,
+                                                 chunk_n=None) -> int:
+    """Device workspace of the block on host buffers (x and out in host memory)."""
+    dt = NRC_F32 if dtype == torch.float32 else NRC_BF16
+    return int(load().nrc_prenorm_dilconv_residual_host_workspace_size(
+        N, C, L, dt, chunk_n or _default_chunk(N)))
+
+
+def _default_chunk(N):
+    return max(1, N // 8)
+
+
+def _host(t, dtype=None):
+    """Contiguous host copy of an optional tensor."""
+    if t is None:
+        return None
+    return t.to(device="cpu", dtype=dtype or t.dtype).contiguous()
+
+
+def _prenorm_host(lib, dev, dt, x, rm, rv, g, b, eps, w, cb, dilation, padding, kernel_size,
+                  out, workspace, stream, chunk_n=None):
+    """The block on host buffers through nrc_prenorm_dilconv_residual_host."""
+    xh = x.contiguous()
+    N, C, L = xh.shape
+    rm, rv, g, b = (_host(t, torch.float32) for t in (rm, rv, g, b))
+    wh, cbh = _host(w, x.dtype), _host(cb, x.dtype)
+    padding = dilation if padding is None else padding
+    chunk_n = chunk_n or _default_chunk(N)
+    need = lib.nrc_prenorm_dilconv_residual_host_workspace_size(N, C, L, dt, chunk_n)
+    if need == 0:
+        raise ValueError("bad shape for the host-buffer block")
+    ws = _workspace(need, dev, workspace)
+    res = out if out is not None else torch.empty(xh.shape, dtype=xh.dtype, pin_memory=True)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    status = lib.nrc_prenorm_dilconv_residual_host(
+        _ptr(xh), _ptr(res), dt, N, C, L, kernel_size, dilation, padding, _ptr(rm), _ptr(rv),
+        _ptr(g), _ptr(b), float(eps), _ptr(wh), _ptr(cbh), int(chunk_n), _ptr(ws),
+        ws.numel(), ctypes.c_void_p(st.cuda_stream))
+    _check(status, "nrc_prenorm_dilconv_residual_host")
+    st.synchronize()                      # out is host memory: valid on return
+    return res
 
 
 def _keep_alive(stream, *tensors):

@@ -730,28 +730,35 @@ extern "C" size_t nrc_prenorm_dilconv_residual_workspace_size(int C, nrc_dtype d
     return plan_conv(1, C, C, 1, dt == NRC_F32 ? 2 : 1, true).wpack_bytes;
 }
 
-extern "C" nrc_status nrc_prenorm_dilconv_residual(
-    const void* x, void* out, nrc_dtype dt, int N, int C, int L, int kernel_size, int dilation,
-    int padding, const float* rm, const float* rv, const float* gamma, const float* beta,
-    float bn_eps, const void* conv_weight, const void* conv_bias, void* workspace,
-    size_t workspace_bytes, void* stream) {
-    if (dt != NRC_F32 && dt != NRC_BF16) return NRC_ERR_INVALID_ARG;
-    if (!x || !out || !rm || !rv || !gamma || !beta || !conv_weight || !workspace)
-        return NRC_ERR_INVALID_ARG;
-    if (N <= 0 || C <= 0 || L <= 0 || dilation <= 0 || padding < 0) return NRC_ERR_INVALID_ARG;
-    if (!(bn_eps >= 0.f) || !std::isfinite(bn_eps)) return NRC_ERR_INVALID_ARG;
-    if (kernel_size != 3 || padding != dilation) return NRC_ERR_UNSUPPORTED;
-    if (C > 2048) return NRC_ERR_UNSUPPORTED;
-    const size_t esz = dt == NRC_F32 ? 4 : 2;
-    const size_t bytes = (size_t)N * C * L * esz;
-    if (ranges_overlap(x, bytes, out, bytes)) return NRC_ERR_INVALID_ARG;
-    if (!aligned(workspace, 16)) return NRC_ERR_ALIGNMENT;
+namespace {
+
+// The block's weight image (packed once per call into wpack; depends on C only).
+nrc_status block_pack(const void* conv_weight, nrc_dtype dt, int C, void* wpack,
+                      cudaStream_t st) {
+    const int NP = dt == NRC_F32 ? 2 : 1;
+    const ConvPlan pl = plan_conv(1, C, C, 1, NP, true);
+    const size_t units = pl.wpack_bytes / 16 / NP;
+    TraceScope ts("pack_conv_weight", st);
+    if (dt == NRC_F32)
+        pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
+            static_cast<const float*>(conv_weight), static_cast<uint8_t*>(wpack), C, C, pl.g.BN,
+            pl.n_ot, pl.n_chunks);
+    else
+        pack_conv_weight_kernel<__nv_bfloat16, 1><<<elementwise_grid(units), 256, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(conv_weight), static_cast<uint8_t*>(wpack), C, C,
+            pl.g.BN, pl.n_ot, pl.n_chunks);
+    return cuda_status(cudaGetLastError());
+}
+
+// Plans and launches the block's GEMM on device buffers; wpack holds the
+// packed weight image.  Arguments already validated.
+nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int L, int dilation,
+                      int padding, const float* rm, const float* rv, const float* gamma,
+                      const float* beta, float bn_eps, const void* conv_bias,
+                      const uint8_t* wpack, cudaStream_t st) {
     const int NP = dt == NRC_F32 ? 2 : 1;
     ConvPlan pl = plan_conv(N, C, C, L, NP, true);
-    if (workspace_bytes < pl.wpack_bytes) return NRC_ERR_WORKSPACE;
     if ((long long)N * pl.n_tt * pl.n_ot >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
-
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     ConvParams p{};
     p.x = x;
     const bool staged = dt == NRC_F32 ? plan_conv_staged<float>(p, pl, N, C, C, L, true)
@@ -775,39 +782,211 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual(
     p.bn_eps = bn_eps;
     p.bias = conv_bias;
     p.bias_off = 2 * pl.n_chunks * kBK;
-    p.wpack = static_cast<const uint8_t*>(workspace);
+    p.wpack = wpack;
     // Residual drain overlapped at tile boundaries (whole 128-column halves).
     if (pl.g.BN % 128 == 0) {
         const int SA = 256 / (32 * NP);
         pl.g.split_h = std::min(std::min(SA, pl.g.b_stages), pl.g.num_kiters / 2);
     }
-    const size_t units = pl.wpack_bytes / 16 / NP;
     if (dt == NRC_F32) {
-        {
-            TraceScope ts("pack_conv_weight", st);
-            pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
-                static_cast<const float*>(conv_weight), static_cast<uint8_t*>(workspace), C, C,
-                pl.g.BN, pl.n_ot, pl.n_chunks);
-        }
-        if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
         if (staged)
             return launch_gemm<ConvProblem<float, ConvEpi::kResidual, true>, 2>(
                 "prenorm_block_gemm", p, pl.g, st);
         return launch_gemm<ConvProblem<float, ConvEpi::kResidual, false>, 2>(
             "prenorm_block_gemm", p, pl.g, st);
     }
-    {
-        TraceScope ts("pack_conv_weight", st);
-        pack_conv_weight_kernel<__nv_bfloat16, 1><<<elementwise_grid(units), 256, 0, st>>>(
-            static_cast<const __nv_bfloat16*>(conv_weight), static_cast<uint8_t*>(workspace), C,
-            C, pl.g.BN, pl.n_ot, pl.n_chunks);
-    }
-    if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
     if (staged)
         return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual, true>, 1>(
             "prenorm_block_gemm", p, pl.g, st);
     return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual, false>, 1>(
         "prenorm_block_gemm", p, pl.g, st);
+}
+
+// Shared argument checks of the block entry points (device or host buffers).
+nrc_status block_check(const void* x, const void* out, nrc_dtype dt, int N, int C, int L,
+                       int kernel_size, int dilation, int padding, const void* rm,
+                       const void* rv, const void* gamma, const void* beta, float bn_eps,
+                       const void* conv_weight, const void* workspace) {
+    if (dt != NRC_F32 && dt != NRC_BF16) return NRC_ERR_INVALID_ARG;
+    if (!x || !out || !rm || !rv || !gamma || !beta || !conv_weight || !workspace)
+        return NRC_ERR_INVALID_ARG;
+    if (N <= 0 || C <= 0 || L <= 0 || dilation <= 0 || padding < 0) return NRC_ERR_INVALID_ARG;
+    if (!(bn_eps >= 0.f) || !std::isfinite(bn_eps)) return NRC_ERR_INVALID_ARG;
+    if (kernel_size != 3 || padding != dilation) return NRC_ERR_UNSUPPORTED;
+    if (C > 2048) return NRC_ERR_UNSUPPORTED;
+    const size_t bytes = (size_t)N * C * L * (dt == NRC_F32 ? 4 : 2);
+    if (ranges_overlap(x, bytes, out, bytes)) return NRC_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return NRC_ERR_ALIGNMENT;
+    return NRC_OK;
+}
+
+}  // namespace
+
+extern "C" nrc_status nrc_prenorm_dilconv_residual(
+    const void* x, void* out, nrc_dtype dt, int N, int C, int L, int kernel_size, int dilation,
+    int padding, const float* rm, const float* rv, const float* gamma, const float* beta,
+    float bn_eps, const void* conv_weight, const void* conv_bias, void* workspace,
+    size_t workspace_bytes, void* stream) {
+    const nrc_status c = block_check(x, out, dt, N, C, L, kernel_size, dilation, padding, rm, rv,
+                                     gamma, beta, bn_eps, conv_weight, workspace);
+    if (c != NRC_OK) return c;
+    if (workspace_bytes < nrc_prenorm_dilconv_residual_workspace_size(C, dt))
+        return NRC_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const nrc_status s = block_pack(conv_weight, dt, C, workspace, st);
+    if (s != NRC_OK) return s;
+    return block_gemm(x, out, dt, N, C, L, dilation, padding, rm, rv, gamma, beta, bn_eps,
+                      conv_bias, static_cast<const uint8_t*>(workspace), st);
+}
+
+// ---------------------------------------------------------------------------
+// Host-buffer entry point: x and out in host memory (pinned for overlap), the
+// small parameters and weights in host memory too.  The batch goes through in
+// chunks of chunk_n samples and two device buffers: the copy-in of chunk j+1,
+// the GEMM of chunk j and the copy-out of chunk j-1 run at once on two
+// library streams and the caller's stream, ordered by events.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct HostLayout {
+    size_t par, w, b, x[2], o[2], total;
+};
+
+HostLayout host_layout(int N, int C, int L, nrc_dtype dt, int chunk_n) {
+    const size_t es = dt == NRC_F32 ? 4 : 2;
+    auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    const size_t chunk = (size_t)chunk_n * C * L * es;
+    HostLayout h{};
+    h.par = up(nrc_prenorm_dilconv_residual_workspace_size(C, dt));
+    h.w = up(h.par + (size_t)4 * C * sizeof(float));
+    h.b = up(h.w + (size_t)C * C * 3 * es);
+    h.x[0] = up(h.b + (size_t)C * es);
+    h.x[1] = up(h.x[0] + chunk);
+    h.o[0] = up(h.x[1] + chunk);
+    h.o[1] = up(h.o[0] + chunk);
+    h.total = h.o[1] + chunk;
+    (void)N;
+    return h;
+}
+
+// Per device: the copy-in and copy-out streams and the events of the pipeline.
+struct HostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start, join, ev_in[2], ev_gemm[2], ev_out[2];
+    bool ready = false;
+};
+std::mutex g_host_mu;
+HostPipe g_host_pipe[64];
+
+nrc_status host_pipe(HostPipe** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NRC_ERR_CUDA;
+    HostPipe& hp = g_host_pipe[dev];
+    if (!hp.ready) {
+        const unsigned f = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.start, f) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.join, f) != cudaSuccess)
+            return NRC_ERR_CUDA;
+        for (int b = 0; b < 2; ++b)
+            if (cudaEventCreateWithFlags(&hp.ev_in[b], f) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.ev_gemm[b], f) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.ev_out[b], f) != cudaSuccess)
+                return NRC_ERR_CUDA;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return NRC_OK;
+}
+
+}  // namespace
+
+extern "C" size_t nrc_prenorm_dilconv_residual_host_workspace_size(int N, int C, int L,
+                                                                   nrc_dtype dt, int chunk_n) {
+    if (N <= 0 || C <= 0 || L <= 0 || chunk_n <= 0 || (dt != NRC_F32 && dt != NRC_BF16))
+        return 0;
+    return host_layout(N, C, L, dt, std::min(chunk_n, N)).total;
+}
+
+extern "C" nrc_status nrc_prenorm_dilconv_residual_host(
+    const void* x_host, void* out_host, nrc_dtype dt, int N, int C, int L, int kernel_size,
+    int dilation, int padding, const float* rm_host, const float* rv_host,
+    const float* gamma_host, const float* beta_host, float bn_eps, const void* weight_host,
+    const void* bias_host, int chunk_n, void* workspace, size_t workspace_bytes, void* stream) {
+    const nrc_status c = block_check(x_host, out_host, dt, N, C, L, kernel_size, dilation,
+                                     padding, rm_host, rv_host, gamma_host, beta_host, bn_eps,
+                                     weight_host, workspace);
+    if (c != NRC_OK) return c;
+    if (chunk_n <= 0) return NRC_ERR_INVALID_ARG;
+    chunk_n = std::min(chunk_n, N);
+    const HostLayout hl = host_layout(N, C, L, dt, chunk_n);
+    if (workspace_bytes < hl.total) return NRC_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return NRC_ERR_ALIGNMENT;
+
+    std::lock_guard<std::mutex> lk(g_host_mu);      // the per-device pipe is shared
+    HostPipe* hp = nullptr;
+    nrc_status s = host_pipe(&hp);
+    if (s != NRC_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t es = dt == NRC_F32 ? 4 : 2;
+    const size_t sample = (size_t)C * L * es;
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // Parameters and weights: copied and packed on the caller's stream.
+    float* par = reinterpret_cast<float*>(ws + hl.par);
+    bool good = ok(cudaMemcpyAsync(par, rm_host, C * sizeof(float), cudaMemcpyHostToDevice, st)) &&
+                ok(cudaMemcpyAsync(par + C, rv_host, C * sizeof(float), cudaMemcpyHostToDevice,
+                                   st)) &&
+                ok(cudaMemcpyAsync(par + 2 * C, gamma_host, C * sizeof(float),
+                                   cudaMemcpyHostToDevice, st)) &&
+                ok(cudaMemcpyAsync(par + 3 * C, beta_host, C * sizeof(float),
+                                   cudaMemcpyHostToDevice, st)) &&
+                ok(cudaMemcpyAsync(ws + hl.w, weight_host, (size_t)C * C * 3 * es,
+                                   cudaMemcpyHostToDevice, st)) &&
+                (!bias_host || ok(cudaMemcpyAsync(ws + hl.b, bias_host, (size_t)C * es,
+                                                  cudaMemcpyHostToDevice, st)));
+    if (!good) return NRC_ERR_CUDA;
+    s = block_pack(ws + hl.w, dt, C, ws, st);
+    if (s != NRC_OK) return s;
+    // The library streams start after everything already on the caller's stream
+    // (the workspace may still be in use by an earlier call).
+    if (!ok(cudaEventRecord(hp->start, st)) || !ok(cudaStreamWaitEvent(hp->in, hp->start, 0)) ||
+        !ok(cudaStreamWaitEvent(hp->out, hp->start, 0)))
+        return NRC_ERR_CUDA;
+    const uint8_t* xh = static_cast<const uint8_t*>(x_host);
+    uint8_t* oh = static_cast<uint8_t*>(out_host);
+    const int n_chunks = (N + chunk_n - 1) / chunk_n;
+    for (int j = 0; j < n_chunks; ++j) {
+        const int b = j & 1;
+        const int n0 = j * chunk_n, cn = std::min(chunk_n, N - n0);
+        const size_t bytes = (size_t)cn * sample;
+        // copy-in: buffer b is free once the GEMM of chunk j-2 has read it
+        if (j >= 2 && !ok(cudaStreamWaitEvent(hp->in, hp->ev_gemm[b], 0))) return NRC_ERR_CUDA;
+        if (!ok(cudaMemcpyAsync(ws + hl.x[b], xh + (size_t)n0 * sample, bytes,
+                                cudaMemcpyHostToDevice, hp->in)) ||
+            !ok(cudaEventRecord(hp->ev_in[b], hp->in)))
+            return NRC_ERR_CUDA;
+        // GEMM: after its copy-in, and after chunk j-2's copy-out read buffer b
+        if (!ok(cudaStreamWaitEvent(st, hp->ev_in[b], 0)) ||
+            (j >= 2 && !ok(cudaStreamWaitEvent(st, hp->ev_out[b], 0))))
+            return NRC_ERR_CUDA;
+        s = block_gemm(ws + hl.x[b], ws + hl.o[b], dt, cn, C, L, dilation, padding, par,
+                       par + C, par + 2 * C, par + 3 * C, bn_eps,
+                       bias_host ? static_cast<const void*>(ws + hl.b) : nullptr, ws, st);
+        if (s != NRC_OK) return s;
+        if (!ok(cudaEventRecord(hp->ev_gemm[b], st))) return NRC_ERR_CUDA;
+        // copy-out
+        if (!ok(cudaStreamWaitEvent(hp->out, hp->ev_gemm[b], 0)) ||
+            !ok(cudaMemcpyAsync(oh + (size_t)n0 * sample, ws + hl.o[b], bytes,
+                                cudaMemcpyDeviceToHost, hp->out)) ||
+            !ok(cudaEventRecord(hp->ev_out[b], hp->out)))
+            return NRC_ERR_CUDA;
+    }
+    // The caller's stream resumes once the last copy-out has landed.
+    if (!ok(cudaEventRecord(hp->join, hp->out)) || !ok(cudaStreamWaitEvent(st, hp->join, 0)))
+        return NRC_ERR_CUDA;
+    return NRC_OK;
 }
 
 static size_t gn_partials_offset(const ConvPlan& pl) {

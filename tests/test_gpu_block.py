@@ -147,3 +147,36 @@ def test_repeat_calls_identical():
     inp = syn.prenorm_block_inputs(2, 128, 640, 32, seed=8)
     a, b = _gpu(dev, inp), _gpu(dev, inp)
     assert np.array_equal(a, b)
+
+
+def _host_call(inp, chunk_n, pinned=True):
+    from normalization_convolution_blocks_gb300 import api
+    x = inp.x.pin_memory() if pinned else inp.x
+    out = api.prenorm_dilconv_residual(x, inp.running_mean, inp.running_var, inp.gamma,
+                                       inp.beta, inp.eps, inp.weight, inp.bias, inp.dilation,
+                                       chunk_n=chunk_n)
+    assert not out.is_cuda and api.query_status() == api.NRC_OK
+    return out.double().numpy()
+
+
+@pytest.mark.parametrize("N,C,L,d,chunk_n,dtype", [
+    (5, 64, 300, 8, 2, torch.float32),       # ragged last chunk, both buffers reused
+    (4, 256, 512, 128, 1, torch.float32),    # one sample per chunk
+    (3, 96, 296, 5, 8, torch.float32),       # chunk larger than the batch
+    (6, 128, 264, 2, 4, torch.bfloat16),     # bf16, two chunks
+])
+def test_host_buffer_entry_matches_device_entry(N, C, L, d, chunk_n, dtype):
+    """The host-buffer entry runs the same GEMM per chunk as the device entry:
+    results must be bitwise equal, and within the parity bar of the oracle."""
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(N, C, L, d, seed=N * 31 + C + d, dtype=dtype)
+    got = _host_call(inp, chunk_n)
+    assert np.array_equal(got, _gpu(dev, inp))
+    check = assert_f32 if dtype == torch.float32 else assert_bf16
+    check(got, _oracle(inp), f"host entry N{N} C{C} chunk {chunk_n}")
+
+
+def test_host_buffer_entry_pageable_input():
+    dev = need_gpu()
+    inp = syn.prenorm_block_inputs(3, 48, 200, 3, seed=44)
+    assert np.array_equal(_host_call(inp, 2, pinned=False), _gpu(dev, inp))
