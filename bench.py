@@ -44,24 +44,31 @@ TF32_PER_BF16 = 1.1 / 2.25        # nominal dense tf32 : bf16 tensor rate on GB3
 L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic (read + write bytes) of one launch of the dominant kernel, from
-# one ncu capture (profiles/), keyed by workload; valid only while the kernel
-# sources hash to the recorded value.
+# one ncu capture (profiles/), keyed by workload; valid only while the sources
+# that define that kernel (its translation unit and the shared headers) hash to
+# the recorded value.
 NCU_TRAFFIC = {
-    "prenorm_block_f32": {"bytes": 221731072, "src_hash": "137fb19427aaca81",
+    "prenorm_block_f32": {"bytes": 221669120, "src_hash": "87554c2bee6d83cf",
                           "profile": "profiles/gemm_prenorm_block_f32_N32_C256_L4096_d128.md"},
-    "linear_bn_swish_f32": {"bytes": 359206144, "src_hash": "137fb19427aaca81",
+    "linear_bn_swish_f32": {"bytes": 358332160, "src_hash": "aaeda32a97438e5c",
                             "profile": "profiles/gemm_linear_bn_swish_f32_B1024_IN8192_OUT8192.md"},
-    "conv1d_groupnorm_f32": {"bytes": 8852736, "src_hash": "137fb19427aaca81",
+    "conv1d_groupnorm_f32": {"bytes": 8857344, "src_hash": "87554c2bee6d83cf",
                              "profile": "profiles/gemm_conv1d_groupnorm_f32_N16_C128_256_T1024_G32.md"},
 }
+KERNEL_TU = {"block": "conv_blocks.cu", "conv_gn": "conv_blocks.cu", "linear": "linear_bn_swish.cu"}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(workload: str) -> str:
+    """Hash of the translation unit defining the workload's kernels plus the
+    shared headers (nrc_*.cuh, nrc_host.h)."""
+    from normalization_convolution_blocks_gb300 import synthetic as syn
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "normalization_convolution_blocks_gb300", "csrc")
+    tu = KERNEL_TU[syn.WORKLOADS[workload].kind]
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        if name == tu or name.endswith((".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -392,7 +399,8 @@ def gpu_arm(args, world, rank, local):
         roof = dict(bound="hbm", achieved=round(achieved, 1), peak=round(hbm_peak, 1),
                     unit="GB/s", frac=round(achieved / hbm_peak, 4))
     tr = NCU_TRAFFIC.get(args.workload)
-    roof["traffic"] = tr["bytes"] if tr and tr["src_hash"] == kernel_source_hash() else None
+    roof["traffic"] = (tr["bytes"] if tr and tr["src_hash"] == kernel_source_hash(args.workload)
+                       else None)
     roof["kernel"] = main
     roof["kernel_ms"] = round(main_ms, 5)
     roof["peak_source"] = f"{peaks_src}: {tensor_note if roof['bound'] == 'tensor' else 'hbm_gbs'}"

@@ -700,7 +700,9 @@ static bool make_x_map(ConvParams& p, const void* x, int N, int Cin, int L, bool
 }
 
 // Plans the conv GEMM, staged when x allows it and the slots fit; fills the
-// map and returns whether the staged kernel runs.
+// map and returns whether the staged kernel runs.  p.x and p.out must be set:
+// the staged bf16 residual epilogue moves x and out in 8-byte words, so it
+// also needs out 8-byte aligned (x is 16-byte aligned for the map).
 template <typename T>
 static bool plan_conv_staged(ConvParams& p, ConvPlan& pl, int N, int Cin, int Cout, int L,
                              bool with_bn) {
@@ -710,7 +712,8 @@ static bool plan_conv_staged(ConvParams& p, ConvPlan& pl, int N, int Cin, int Co
     const uint32_t stage_bytes =
         (with_bn && sizeof(T) == 2) ? 2u * ConvProblem<T, ConvEpi::kResidual, true>::kChunkBufBytes
                                     : 0u;
-    if (make_x_map<T>(p, p.x, N, Cin, L, with_bn)) {
+    const bool out_ok = !(with_bn && sizeof(T) == 2) || aligned(p.out, 8);
+    if (out_ok && make_x_map<T>(p, p.x, N, Cin, L, with_bn)) {
         pl = plan_conv(N, Cin, Cout, L, NP, with_bn, box_bytes, stage_bytes);
         if (pl.g.b_stages >= 2 && pl.g.x_depth >= 2) {
             p.stage_off = pl.stage_off;
@@ -761,9 +764,9 @@ nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int 
     if ((long long)N * pl.n_tt * pl.n_ot >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
     ConvParams p{};
     p.x = x;
+    p.out = out;
     const bool staged = dt == NRC_F32 ? plan_conv_staged<float>(p, pl, N, C, C, L, true)
                                       : plan_conv_staged<__nv_bfloat16>(p, pl, N, C, C, L, true);
-    p.out = out;
     p.N = N;
     p.Cin = C;
     p.Cout = C;
@@ -1029,8 +1032,8 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     ConvParams p{};
     p.x = x;
-    const bool staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
     p.out = out;
+    const bool staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
     p.N = N;
     p.Cin = C_in;
     p.Cout = C_out;

@@ -180,3 +180,29 @@ def test_host_buffer_entry_pageable_input():
     dev = need_gpu()
     inp = syn.prenorm_block_inputs(3, 48, 200, 3, seed=44)
     assert np.array_equal(_host_call(inp, 2, pinned=False), _gpu(dev, inp))
+
+
+@pytest.mark.parametrize("which", ["out", "x"])
+def test_bf16_views_at_odd_offsets(which):
+    """x or out starting 2 bytes past an 8-byte boundary: the staged bf16 path
+    (16-byte TMA boxes of x, 8-byte residual/output words) must not be taken,
+    and the result must still match the oracle."""
+    dev = need_gpu()
+    from normalization_convolution_blocks_gb300 import api
+    inp = syn.prenorm_block_inputs(2, 64, 256, 4, seed=17, dtype=torch.bfloat16)
+    n = inp.x.numel()
+    x = to(dev, inp.x)
+    out = None
+    if which == "x":
+        xb = torch.empty(n + 1, dtype=torch.bfloat16, device=dev)
+        xb[1:].copy_(x.reshape(-1))
+        x = xb[1:].view(inp.x.shape)
+    else:
+        out = torch.empty(n + 1, dtype=torch.bfloat16, device=dev)[1:].view(inp.x.shape)
+    assert (x if which == "x" else out).data_ptr() % 8 == 2
+    got = api.prenorm_dilconv_residual(x, to(dev, inp.running_mean), to(dev, inp.running_var),
+                                       to(dev, inp.gamma), to(dev, inp.beta), inp.eps,
+                                       to(dev, inp.weight), to(dev, inp.bias), inp.dilation,
+                                       out=out)
+    assert api.query_status() == api.NRC_OK
+    assert_bf16(got.double().cpu().numpy(), _oracle(inp), f"bf16 {which} at +2 bytes")
