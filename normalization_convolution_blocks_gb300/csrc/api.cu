@@ -18,6 +18,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 int* g_status_addr[kMaxDevices];
 int g_sm_count[kMaxDevices];
+int g_coop[kMaxDevices];         // 0 unknown, 1 supported, 2 not
 std::mutex g_mu;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 int g_last_site = 0;
@@ -53,6 +54,18 @@ int device_sm_count() {
         g_sm_count[d] = n > 0 ? n : 1;
     }
     return g_sm_count[d];
+}
+
+bool device_coop_launch() {
+    const int d = current_device();
+    if (d < 0) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_coop[d]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, d);
+        g_coop[d] = v ? 1 : 2;
+    }
+    return g_coop[d] == 1;
 }
 
 namespace {

@@ -64,7 +64,33 @@ struct ConvParams {
     float2* partials;       // [((n*G + g) * n_tt + tt) * 128 + row] = (mean, M2) of the
                             // row's cpg values (count cpg, or 0 for rows past L)
     int G, cpg;
+    // conv + GroupNorm in one wave (fused): every tile on its own resident CTA
+    int fused;
+    uint32_t* grid_counter;  // zeroed before the launch; one arrival per CTA
+    float4* tile_stats;      // [(n*G + g) * n_tt + tt] = (count, mean, M2, 0) of a tile's group
+    const float *gn_gamma, *gn_beta;
+    float gn_eps;
+    int* status;             // device status word, for the grid barrier's give-up
+    unsigned long long timeout_ns;
 };
+
+// Shared memory of the fused conv + GroupNorm epilogue: per-warp group
+// partials [group][4] (float4), then the per-channel scale and shift.
+constexpr int kGnMaxGroups = 256;
+constexpr uint32_t kGnFusedBytes = kGnMaxGroups * 4 * 16 + 2 * 256 * 4;
+
+// Chan's pairwise merge of (count, mean, M2) b into a.
+__device__ __forceinline__ void chan_merge(float& cnt, float& mean, float& m2, float nb, float mb,
+                                           float qb) {
+    const float nab = cnt + nb;
+    if (nab > 0.f) {
+        const float delta = mb - mean;
+        const float fb = nb / nab;
+        mean += delta * fb;
+        m2 += qb + delta * delta * cnt * fb;
+        cnt = nab;
+    }
+}
 
 // Tile index -> (n, t tile, o tile); o tiles of one (n, t) are adjacent, then t,
 // so neighbouring CTAs share the x windows (and the +-dil halos) in L2.
@@ -126,6 +152,82 @@ __device__ __forceinline__ void gn_chunk_stats(const float (&v)[16], int n, floa
     }
 }
 
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// TMEM load of COLS (16, 32 or 64) consecutive columns, one wait.
+template <int COLS>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[COLS]) {
+    if constexpr (COLS == 16)
+        tmem_ld16(taddr, v);
+    else if constexpr (COLS == 32)
+        tmem_ld32(taddr, v);
+    else
+        tmem_ld64(taddr, v);
+}
+
+// Fused GroupNorm, step 1 for groups of CPG channels (CPG divides 16): the
+// accumulator is read COLS columns at a time (one TMEM round trip); for each
+// of the NB whole groups in them, the row's mean and M2 over its CPG values
+// (two-pass), then the warp's (count, mean, M2) over its valid rows by two
+// warp sums, the NB groups' sums interleaved so their shuffle latencies
+// overlap.  Lane 0 writes s_part[local group][quarter].
+template <int CPG>
+__device__ __forceinline__ void gn_tile_stats(const float* bias_s, uint32_t taddr, int ovalid,
+                                              int ng, float tw, float inv_nvr, float wcount,
+                                              int quarter, int lane, float4* s_part) {
+    constexpr int COLS = CPG == 1 ? 16 : (CPG <= 4 ? 32 : 64);
+    constexpr int NB = COLS / CPG;                      // groups per batch
+    for (int cb = 0; cb < ovalid; cb += COLS) {         // COLS divides 256: no batch
+        float v[COLS];                                  // crosses the accumulator
+        tmem_ld_cols<COLS>(taddr + (uint32_t)cb, v);
+#pragma unroll
+        for (int i = 0; i < COLS; ++i) v[i] = cb + i < ovalid ? v[i] + bias_s[cb + i] : 0.f;
+        float m[NB], q[NB];
+#pragma unroll
+        for (int k = 0; k < NB; ++k) {
+            float s1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPG; ++i) s1 += v[k * CPG + i];
+            m[k] = s1 * (1.0f / CPG);
+            float s2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPG; ++i) {
+                const float d = v[k * CPG + i] - m[k];
+                s2 = fmaf(d, d, s2);
+            }
+            q[k] = s2;
+        }
+        float S[NB];
+#pragma unroll
+        for (int k = 0; k < NB; ++k) S[k] = m[k] * tw;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int k = 0; k < NB; ++k) S[k] += __shfl_xor_sync(0xffffffffu, S[k], off);
+#pragma unroll
+        for (int k = 0; k < NB; ++k) {
+            S[k] *= inv_nvr;                            // the warp's mean of the group
+            const float d = m[k] - S[k];
+            q[k] = tw * (q[k] + (float)CPG * d * d);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int k = 0; k < NB; ++k) q[k] += __shfl_xor_sync(0xffffffffu, q[k], off);
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                const int gl = cb / CPG + k;
+                if (gl < ng) s_part[gl * 4 + quarter] = make_float4(wcount, S[k], q[k], 0.f);
+            }
+        }
+    }
+}
+
 template <typename T, ConvEpi EPI, bool STAGED>
 struct ConvProblem {
     using Params = ConvParams;
@@ -149,6 +251,17 @@ struct ConvProblem {
         // (32 zero floats past the last tile, so vector reads never leave the region)
         for (int o = threadIdx.x; o < p.n_ot * p.BN + 32; o += blockDim.x)
             ex[p.bias_off + o] = (bias && o < p.Cout) ? load_f<T>(bias + o) : 0.f;
+        if (EPI == ConvEpi::kGroupStats && p.fused) {
+            // one tile per CTA: its channels' gamma and beta, staged while the
+            // mainloop runs (the epilogue turns them into scale and shift)
+            const int obase = conv_tile(p, (int)blockIdx.x).ot * p.BN;
+            float* s_a = reinterpret_cast<float*>(extra + p.stage_off + kGnMaxGroups * 4 * 16);
+            for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+                const int o = obase + c;
+                s_a[c] = (p.gn_gamma && o < p.Cout) ? p.gn_gamma[o] : 1.f;
+                s_a[256 + c] = (p.gn_beta && o < p.Cout) ? p.gn_beta[o] : 0.f;
+            }
+        }
         if (p.rm == nullptr) return;
         // BN fold: z = max(0, x*scale + shift), scale = gamma/sqrt(rv+eps),
         // shift = beta - rm*scale.  Channels past Cin get 0.
@@ -430,6 +543,11 @@ struct ConvProblem {
             // is uniform across the warp except t_ok (invalid rows count 0).
             for (int h = 0; h < halves; ++h)
                 if (!acquire(h)) return false;
+            if (p.fused) {
+                const bool ok = gn_fused(p, extra, tl, quarter, lane, taddr, BN);
+                for (int h = 0; h < halves; ++h) release(h);
+                return ok;
+            }
             const int ovalid = p.Cout - obase;
             float cnt = 0.f, mean = 0.f, m2 = 0.f;
             const float tw = t_ok ? 1.f : 0.f;
@@ -524,6 +642,169 @@ struct ConvProblem {
                 }
             }
             for (int h = 0; h < halves; ++h) release(h);
+        }
+        return true;
+    }
+
+    // Conv + GroupNorm when every tile has its own CTA and all are resident
+    // (cooperative launch): y = acc + bias never leaves TMEM.
+    //  1. Each group's (count, mean, M2) over the tile: per row two-pass over
+    //     the group's run of channels, merged over the warp's 32 rows with
+    //     shuffles, then over the four epilogue warps in shared memory (fixed
+    //     order), written once per (n, group, t tile).
+    //  2. Grid-wide barrier: one arrival per CTA on a counter zeroed before
+    //     the launch; one thread waits for all (bounded).
+    //  3. Each group's statistics merged over the sample's n_tt tiles, in t
+    //     order, so every CTA of the sample computes the same values; scale
+    //     a = gamma*rsqrt(var + eps) and shift beta - mean*a per channel.
+    //  4. out = y*a + shift, read again from TMEM.
+    // The four epilogue warps meet at named barrier 1.  Tiles hold whole groups.
+    static __device__ bool gn_fused(const Params& p, const uint8_t* extra, const Tile& tl,
+                                    int quarter, int lane, uint32_t taddr, int BN) {
+        const int t = tl.tt * kBM + quarter * 32 + lane;
+        const bool t_ok = t < p.L;
+        const float tw = t_ok ? 1.f : 0.f;
+        const int obase = tl.ot * BN;
+        const int ovalid = min(BN, p.Cout - obase);
+        const int ng = ovalid / p.cpg;                 // groups of this tile
+        const int g0 = obase / p.cpg;
+        const int etid = quarter * 32 + lane;          // 0..127 over the four warps
+        const float* bias_s = reinterpret_cast<const float*>(extra) + p.bias_off + obase;
+        uint8_t* ex = const_cast<uint8_t*>(extra) + p.stage_off;
+        float4* s_part = reinterpret_cast<float4*>(ex);                 // [group][warp]
+        float* s_a = reinterpret_cast<float*>(ex + kGnMaxGroups * 4 * 16);
+        float* s_sh = s_a + 256;
+
+        // 1. group statistics of the tile.  Every valid row of a group has the
+        //    same count (cpg), so the warp's merge of its rows is two warp sums:
+        //    of the row means, then of M2_r + cpg*(mean_r - mean)^2.
+        const int nvr = __popc(__ballot_sync(0xffffffffu, t_ok));   // valid rows of the warp
+        const float inv_nvr = nvr > 0 ? 1.f / (float)nvr : 0.f;
+        const float wcount = (float)(p.cpg * nvr);
+        switch (p.cpg) {
+            case 1: gn_tile_stats<1>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part); break;
+            case 2: gn_tile_stats<2>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part); break;
+            case 4: gn_tile_stats<4>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part); break;
+            case 8: gn_tile_stats<8>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part); break;
+            case 16: gn_tile_stats<16>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part); break;
+            default: {
+                // groups crossing 16-channel chunks: each row's (count, mean, M2)
+                // over the group's runs, then the warp sums at its last run
+                float cnt = 0.f, mean = 0.f, m2 = 0.f;
+                int gend = obase + p.cpg;              // first channel after the group
+                for (int cc = 0; cc < ovalid; cc += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + (uint32_t)cc, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] += bias_s[cc + i];
+                    const int n = min(16, ovalid - cc);
+                    int i0 = 0;
+                    while (i0 < n) {                    // runs [i0, i1) of one group
+                        const int i1 = min(n, gend - (obase + cc));
+                        float s1 = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) s1 += (i >= i0 && i < i1) ? v[i] : 0.f;
+                        const float k = (float)(i1 - i0);
+                        const float rm = s1 / k;
+                        float sq = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float d = (i >= i0 && i < i1) ? v[i] - rm : 0.f;
+                            sq = fmaf(d, d, sq);
+                        }
+                        chan_merge(cnt, mean, m2, k, rm, sq);
+                        if (obase + cc + i1 == gend) {  // group complete (uniform)
+                            const float wm = warp_sum(mean * tw) * inv_nvr;
+                            const float d = mean - wm;
+                            const float wq = warp_sum(tw * (m2 + (float)p.cpg * d * d));
+                            if (lane == 0)
+                                s_part[(gend / p.cpg - 1 - g0) * 4 + quarter] =
+                                    make_float4(wcount, wm, wq, 0.f);
+                            gend += p.cpg;
+                            cnt = 0.f;
+                            mean = 0.f;
+                            m2 = 0.f;
+                        }
+                        i0 = i1;
+                    }
+                }
+            }
+        }
+        named_bar_sync(1, 128);
+        for (int gl = etid; gl < ng; gl += 128) {
+            float c = 0.f, m = 0.f, q = 0.f;
+            for (int w = 0; w < 4; ++w) {
+                const float4 sp = s_part[gl * 4 + w];
+                chan_merge(c, m, q, sp.x, sp.y, sp.z);
+            }
+            p.tile_stats[((size_t)tl.n * p.G + g0 + gl) * p.n_tt + tl.tt] = make_float4(c, m, q, 0.f);
+        }
+        // (s_a and s_sh hold the channels' gamma and beta, staged by setup)
+        __threadfence();
+        named_bar_sync(1, 128);
+
+        // 2. grid-wide barrier
+        bool ok = true;
+        if (etid == 0) {
+            __threadfence();
+            atomicAdd(p.grid_counter, 1u);
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(p.grid_counter) < gridDim.x) {
+                if (globaltimer_ns() - t0 > p.timeout_ns) {
+                    record_status(p.status, kStatusTimeout, kSiteGridBarrier);
+                    ok = false;
+                    break;
+                }
+                __nanosleep(128);
+            }
+        }
+        if (!named_bar_and(1, 128, ok)) return false;
+
+        // 3. the sample's statistics of each group of the tile
+        for (int gl = etid; gl < ng; gl += 128) {
+            const int g = g0 + gl;
+            float c = 0.f, m = 0.f, q = 0.f;
+            const float4* ts = p.tile_stats + ((size_t)tl.n * p.G + g) * p.n_tt;
+            for (int t0 = 0; t0 < p.n_tt; t0 += 8) {      // eight loads in flight
+                float4 sp[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    sp[k] = t0 + k < p.n_tt ? __ldcg(ts + t0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) chan_merge(c, m, q, sp[k].x, sp[k].y, sp[k].z);
+            }
+            const float var = fmaxf(q / c, 0.f);      // biased variance
+            const float inv = 1.0f / sqrtf(var + p.gn_eps);
+            for (int i = 0; i < p.cpg; ++i) {
+                const int cl = gl * p.cpg + i;             // channel within the tile
+                const float a = inv * s_a[cl];
+                s_a[cl] = a;
+                s_sh[cl] = s_sh[cl] - m * a;
+            }
+        }
+        named_bar_sync(1, 128);
+
+        // 4. normalize from TMEM, 64 columns per round trip
+        T* out = static_cast<T*>(p.out);
+        T* op0 = out + ((size_t)tl.n * p.Cout + obase) * p.L + t;
+        for (int cb = 0; cb < ovalid; cb += 64) {          // 64 divides 256
+            float v[64];
+            tmem_ld64(taddr + (uint32_t)cb, v);
+            T* op = op0 + (size_t)cb * p.L;
+            if (cb + 64 <= ovalid) {
+                if (t_ok) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        store_f<T>(op + (size_t)i * p.L,
+                                   fmaf(v[i] + bias_s[cb + i], s_a[cb + i], s_sh[cb + i]));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (t_ok && cb + i < ovalid)
+                        store_f<T>(op + (size_t)i * p.L,
+                                   fmaf(v[i] + bias_s[cb + i], s_a[cb + i], s_sh[cb + i]));
+            }
         }
         return true;
     }
@@ -708,10 +989,12 @@ static bool plan_conv_staged(ConvParams& p, ConvPlan& pl, int N, int Cin, int Co
                              bool with_bn) {
     constexpr int NP = sizeof(T) == 4 ? 2 : 1;
     constexpr uint32_t box_bytes = (uint32_t)((kBM + 16 / sizeof(T)) * kBK * sizeof(T));
-    // the staged bf16 residual epilogue needs its two chunk buffers
+    // the staged bf16 residual epilogue needs its two chunk buffers, the fused
+    // GroupNorm epilogue its partials and per-channel scale and shift
+    const uint32_t fused_bytes = p.fused ? kGnFusedBytes : 0u;
     const uint32_t stage_bytes =
         (with_bn && sizeof(T) == 2) ? 2u * ConvProblem<T, ConvEpi::kResidual, true>::kChunkBufBytes
-                                    : 0u;
+                                    : fused_bytes;
     const bool out_ok = !(with_bn && sizeof(T) == 2) || aligned(p.out, 8);
     if (out_ok && make_x_map<T>(p, p.x, N, Cin, L, with_bn)) {
         pl = plan_conv(N, Cin, Cout, L, NP, with_bn, box_bytes, stage_bytes);
@@ -720,7 +1003,8 @@ static bool plan_conv_staged(ConvParams& p, ConvPlan& pl, int N, int Cin, int Co
             return true;
         }
     }
-    pl = plan_conv(N, Cin, Cout, L, NP, with_bn);
+    pl = plan_conv(N, Cin, Cout, L, NP, with_bn, 0, fused_bytes);
+    p.stage_off = pl.stage_off;
     return false;
 }
 
@@ -1033,6 +1317,9 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     ConvParams p{};
     p.x = x;
     p.out = out;
+    // One wave (every tile on its own CTA, all resident): the GroupNorm is
+    // finished inside the GEMM kernel behind a grid-wide barrier.
+    p.fused = (pl.g.num_tiles <= device_sm_count() && device_coop_launch()) ? 1 : 0;
     const bool staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
     p.N = N;
     p.Cin = C_in;
@@ -1058,12 +1345,26 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
             conv_weight, ws, C_out, C_in, pl.g.BN, pl.n_ot, pl.n_chunks);
     }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
+    if (p.fused) {
+        uint8_t* part = ws + gn_partials_offset(pl);
+        p.grid_counter = reinterpret_cast<uint32_t*>(part);
+        p.tile_stats = reinterpret_cast<float4*>(part + 256);
+        p.gn_gamma = gn_gamma;
+        p.gn_beta = gn_beta;
+        p.gn_eps = eps;
+        p.status = device_status_ptr();
+        p.timeout_ns = wait_timeout_ns();
+        if (p.status == nullptr) return NRC_ERR_CUDA;
+        if (cudaMemsetAsync(p.grid_counter, 0, sizeof(uint32_t), st) != cudaSuccess)
+            return NRC_ERR_CUDA;
+        pl.g.coop = true;
+    }
     nrc_status s =
         staged ? launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true>, 2>("conv_gn_gemm",
                                                                                p, pl.g, st)
                : launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, false>, 2>(
                      "conv_gn_gemm", p, pl.g, st);
-    if (s != NRC_OK) return s;
+    if (s != NRC_OK || p.fused) return s;
     {
         TraceScope ts("groupnorm_finalize_normalize", st);
         groupnorm_finalize_normalize_kernel<<<N * num_groups, 256, 0, st>>>(

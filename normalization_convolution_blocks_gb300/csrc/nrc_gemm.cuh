@@ -60,7 +60,7 @@ constexpr uint32_t kTmemARing = 256;           // first column of the A ring
 
 enum WaitSite : int {
     kSiteBEmpty = 1, kSiteAEmpty = 2, kSiteAccEmpty = 3, kSiteFullA = 4, kSiteFullB = 5,
-    kSiteAccFull = 6, kSiteFullX = 7, kSiteEmptyX = 8
+    kSiteAccFull = 6, kSiteFullX = 7, kSiteEmptyX = 8, kSiteGridBarrier = 9
 };
 
 struct GemmCfg {

@@ -16,6 +16,8 @@ int* device_status_ptr();
 unsigned long long wait_timeout_ns();
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+// Whether the current device supports cooperative launches (cached per device).
+bool device_coop_launch();
 
 // Encodes a 3-D tiled tensor map (dims and box innermost first, strides in
 // bytes of dims 1 and 2) through the driver's cuTensorMapEncodeTiled, reached

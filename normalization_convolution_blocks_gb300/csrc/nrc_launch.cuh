@@ -13,6 +13,7 @@ namespace nrc {
 struct GemmPlan {
     int BN, num_tiles, num_kiters, b_stages, x_depth;
     int split_h;            // accumulator handed over in column halves, H stages (0: whole)
+    bool coop;              // cooperative launch, one CTA per tile (all resident at once)
     uint32_t b_stage_bytes, x_box_bytes, extra_bytes, smem_bytes;
 };
 
@@ -84,6 +85,25 @@ inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
     cfg.timeout_ns = wait_timeout_ns();
     if (cfg.status == nullptr) return NRC_ERR_CUDA;
     // Each CTA allocates all 512 TMEM columns, so one CTA per SM.
+    if (pl.coop) {
+        // every tile on its own CTA, all resident (the kernel synchronises the
+        // grid): the driver refuses the launch if they cannot be
+        if (pl.num_tiles > device_sm_count() || !device_coop_launch()) return NRC_ERR_UNSUPPORTED;
+        cudaLaunchConfig_t lc{};
+        lc.gridDim = dim3((unsigned)pl.num_tiles);
+        lc.blockDim = dim3(kThreads);
+        lc.dynamicSmemBytes = pl.smem_bytes;
+        lc.stream = stream;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeCooperative;
+        at[0].val.cooperative = 1;
+        lc.attrs = at;
+        lc.numAttrs = 1;
+        TraceScope ts(name, stream);
+        const cudaError_t e = cudaLaunchKernelEx(&lc, kern, p, cfg);
+        if (e != cudaSuccess) return cuda_status(e);
+        return cuda_status(cudaGetLastError());
+    }
     const int grid = std::min(pl.num_tiles, device_sm_count());
     {
         TraceScope ts(name, stream);

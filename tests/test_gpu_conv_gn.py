@@ -47,6 +47,22 @@ def test_shapes(N, Cin, Cout, T, G):
     assert_f32(_gpu(dev, g, G), _ref(g, G), f"N{N} {Cin}->{Cout} T{T} G{G}")
 
 
+# More tiles than SMs: the two-kernel path (per-row partials, then the
+# finalize+normalize kernel).  The shapes above fit one wave of resident CTAs
+# and take the fused path (statistics exchanged behind a grid-wide barrier,
+# the normalization applied from tensor memory).
+@pytest.mark.parametrize("N,Cin,Cout,T,G", [
+    (4, 16, 64, 5000, 8),     # 160 tiles, ragged T
+    (2, 16, 512, 5000, 32),   # 160 tiles over two output tiles
+])
+def test_shapes_more_tiles_than_sms(N, Cin, Cout, T, G):
+    dev = need_gpu()
+    n_tiles = N * -(-T // 128) * -(-Cout // 256)
+    assert n_tiles > torch.cuda.get_device_properties(dev).multi_processor_count
+    g = syn.conv_groupnorm_inputs(N, Cin, Cout, T, G, seed=Cin + Cout + T + 1)
+    assert_f32(_gpu(dev, g, G), _ref(g, G), f"N{N} {Cin}->{Cout} T{T} G{G}")
+
+
 def test_bias_and_no_affine():
     dev = need_gpu()
     g = syn.conv_groupnorm_inputs(2, 32, 64, 200, 8, seed=3)
