@@ -243,20 +243,20 @@ struct ConvProblem {
         return conv_tile(p, tile);
     }
 
-    static __device__ void setup(const Params& p, uint8_t* extra) {
+    static __device__ void setup(const Params& p, uint8_t* extra, int tid, int nthr) {
         float* ex = reinterpret_cast<float*>(extra);
         // Conv bias for every (padded) output channel, staged once per CTA so
         // the epilogue reads it from shared memory.
         const T* bias = static_cast<const T*>(p.bias);
         // (32 zero floats past the last tile, so vector reads never leave the region)
-        for (int o = threadIdx.x; o < p.n_ot * p.BN + 32; o += blockDim.x)
+        for (int o = tid; o < p.n_ot * p.BN + 32; o += nthr)
             ex[p.bias_off + o] = (bias && o < p.Cout) ? load_f<T>(bias + o) : 0.f;
         if (EPI == ConvEpi::kGroupStats && p.fused) {
             // one tile per CTA: its channels' gamma and beta, staged while the
             // mainloop runs (the epilogue turns them into scale and shift)
             const int obase = conv_tile(p, (int)blockIdx.x).ot * p.BN;
             float* s_a = reinterpret_cast<float*>(extra + p.stage_off + kGnMaxGroups * 4 * 16);
-            for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+            for (int c = tid; c < 256; c += nthr) {
                 const int o = obase + c;
                 s_a[c] = (p.gn_gamma && o < p.Cout) ? p.gn_gamma[o] : 1.f;
                 s_a[256 + c] = (p.gn_beta && o < p.Cout) ? p.gn_beta[o] : 0.f;
@@ -267,7 +267,7 @@ struct ConvProblem {
         // shift = beta - rm*scale.  Channels past Cin get 0.
         float* sc = ex;
         float* sh = sc + p.n_chunks * kBK;
-        for (int c = threadIdx.x; c < p.n_chunks * kBK; c += blockDim.x) {
+        for (int c = tid; c < p.n_chunks * kBK; c += nthr) {
             float sv = 0.f, h = 0.f;
             if (c < p.Cin) {
                 sv = p.gamma[c] / sqrtf(p.rv[c] + p.bn_eps);

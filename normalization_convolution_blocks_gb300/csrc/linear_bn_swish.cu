@@ -53,7 +53,7 @@ struct LinearProblem {
         return Tile{tile / p.n_bt, tile % p.n_bt};
     }
 
-    static __device__ void setup(const Params&, uint8_t*) {}
+    static __device__ void setup(const Params&, uint8_t*, int, int) {}
 
     static __device__ __forceinline__ void load_a(const Params& p, const Tile& tl, int kiter,
                                                   int row, int k0, float (&v)[32]) {

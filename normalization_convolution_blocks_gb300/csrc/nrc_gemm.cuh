@@ -102,7 +102,9 @@ __device__ __forceinline__ void split_store_a(uint32_t taddr_hi, const float (&v
 // Prob must provide:
 //   struct Params; struct Tile;
 //   static __device__ Tile tile_info(const Params&, int tile)
-//   static __device__ void setup(const Params&, uint8_t* extra)        (all threads)
+//   static __device__ void setup(const Params&, uint8_t* extra, int tid, int nthreads)
+//        -> stages the block's parameters in the extra bytes; run by warps 1-13
+//           (tid in [0, nthreads)) while the copy warps issue the first stages
 //   static __device__ void load_a(const Params&, const Tile&, int kiter, int row, int k0,
 //                                 float (&v)[32])
 //        -> issues the loads of the raw values A[row][kiter*64 + k0 .. +32)
@@ -187,15 +189,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    Prob::setup(p, extra);
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+    __syncthreads();                              // barriers initialised
+    // The copy warps (0 and 14) start at once; the others stage the block's
+    // parameters and allocate TMEM meanwhile, then meet at named barrier 2.
+    uint32_t tmem_base = 0;
+    if (warp != 0 && warp != 14) {
+        Prob::setup(p, extra, (int)threadIdx.x - 32, kThreads - 64);
+        if (warp == 1) {
+            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        named_bar_sync(2, kThreads - 64);
+        tc_fence_after();
+        tmem_base = *tmem_slot;
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
         // ------------------------------------------------------------ B producer
