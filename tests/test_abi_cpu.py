@@ -132,3 +132,40 @@ def test_binding_fails_loudly_without_gpu():
     with pytest.raises(RuntimeError):
         api.prenorm_dilconv_residual(inp.x, inp.running_mean, inp.running_var, inp.gamma,
                                      inp.beta, inp.eps, inp.weight, inp.bias, inp.dilation)
+
+
+def _host(lib, **kw):
+    a = dict(x=FAKE, out=FAKE2, dt=0, N=4, C=32, L=64, k=3, d=4, pad=4, rm=FAKE, rv=FAKE,
+             g=FAKE, b=FAKE, eps=1e-5, w=FAKE, bias=FAKE, chunk=2, ws=ctypes.c_void_p(0x30000000),
+             wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.nrc_prenorm_dilconv_residual_host(
+        a["x"], a["out"], a["dt"], a["N"], a["C"], a["L"], a["k"], a["d"], a["pad"], a["rm"],
+        a["rv"], a["g"], a["b"], a["eps"], a["w"], a["bias"], a["chunk"], a["ws"], a["wsb"],
+        a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), 1), (dict(out=None), 1), (dict(w=None), 1), (dict(chunk=0), 1),
+    (dict(dt=7), 1), (dict(N=0), 1), (dict(k=5), 2), (dict(pad=3), 2),
+    (dict(out=ctypes.c_void_p(0x10000000 + 64)), 1),          # out overlaps x
+    (dict(ws=ctypes.c_void_p(0x30000004)), 3),                 # workspace not 16-byte aligned
+    (dict(ws=ctypes.c_void_p(0x30000010)), 3),                 # nor 256-byte aligned
+    (dict(wsb=4096), 4),                                       # workspace too small
+])
+def test_host_buffer_block_validation(lib, kw, expect):
+    """The host-buffer entry rejects bad arguments before any CUDA call."""
+    assert _host(lib, **kw) == expect
+
+
+def test_host_buffer_workspace_query(lib):
+    f = lib.nrc_prenorm_dilconv_residual_host_workspace_size
+    one = f(32, 256, 4096, 0, 1)
+    four = f(32, 256, 4096, 0, 4)
+    # packed weights and parameters, plus two x and two out buffers of a chunk
+    chunk_bytes = 256 * 4096 * 4
+    assert four - one == 4 * 3 * chunk_bytes
+    assert one > 4 * chunk_bytes
+    assert f(32, 256, 4096, 0, 64) == f(32, 256, 4096, 0, 32)      # chunk capped at N
+    assert f(32, 256, 4096, 1, 4) < four                          # bf16 halves the buffers
+    assert f(0, 256, 4096, 0, 4) == 0 and f(32, 256, 4096, 0, 0) == 0 and f(4, 8, 8, 9, 1) == 0
