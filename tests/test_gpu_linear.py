@@ -48,6 +48,27 @@ def test_training_shapes(B, IN, OUT, affine):
     _check(_gpu(dev, li), _ref(li), f"B{B} IN{IN} OUT{OUT}")
 
 
+# More tiles (128 features x 256 batch rows) than SMs, not a whole number of
+# waves: persistent CTAs take a second, partial round of tiles.  Checked on
+# sampled columns (every batch row) and their running statistics.
+@pytest.mark.parametrize("B,IN,OUT", [
+    (256, 128, 20480),        # 160 tiles of 2 K stages
+    (300, 1000, 10000),       # 79 x 2 tiles, ragged batch tile and K
+])
+def test_multi_wave_shapes_sampled_columns(B, IN, OUT):
+    dev = need_gpu()
+    n_tiles = -(-OUT // 128) * -(-B // 256)
+    assert n_tiles > torch.cuda.get_device_properties(dev).multi_processor_count
+    li = syn.linear_bn_swish_inputs(B, IN, OUT, seed=B + IN, random_affine=True)
+    out, rm, rv = _gpu(dev, li)
+    cols = np.unique(np.concatenate([[0, 127, 128, OUT - 1],
+                                     np.random.default_rng(B).integers(0, OUT, 252)]))
+    r_out, r_rm, r_rv, _ = _ref(li, cols=cols)
+    assert_f32(out[:, cols], r_out, f"multi-wave B{B} IN{IN} OUT{OUT}")
+    assert np.abs(rm[cols] - r_rm[cols]).max() < RUNNING_STAT_ABS
+    assert np.abs(rv[cols] - r_rv[cols]).max() < RUNNING_STAT_ABS
+
+
 def test_eval_mode_and_divide():
     dev = need_gpu()
     li = syn.linear_bn_swish_inputs(48, 160, 96, seed=4, random_affine=True)
