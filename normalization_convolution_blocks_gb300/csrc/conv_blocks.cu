@@ -60,6 +60,12 @@ struct ConvParams {
     int bias_off;           // float offset of the staged bias in the extra smem
     int stage_off;          // byte offset of the bf16 epilogue's two chunk buffers (staged bf16)
     const uint8_t* wpack;   // packed weight image
+    // in-kernel weight repack (pack_counter != NULL): every CTA packs a share of
+    // the image from w_raw during setup, then arrives on pack_counter (zeroed
+    // before the launch); the B producer waits for all CTAs (cooperative launch)
+    const void* w_raw;
+    uint8_t* wpack_out;
+    uint32_t* pack_counter;
     // group statistics (conv + GroupNorm)
     float2* partials;       // [((n*G + g) * n_tt + tt) * 128 + row] = (mean, M2) of the
                             // row's cpg values (count cpg, or 0 for rows past L)
@@ -104,6 +110,47 @@ __device__ __forceinline__ ConvTile conv_tile(const ConvParams& p, int tile) {
     r.tt = rest % p.n_tt;
     r.n = rest / p.n_tt;
     return r;
+}
+
+// One 16-byte chunk of the weight image: W (Cout, Cin, 3) -> for each (o tile,
+// tap, 64-channel chunk) the B-stage image, NP parts of BN rows x 64 bf16,
+// 128B-swizzled (fp32 split into hi + lo bf16; bf16 copied).  Rows past Cout
+// and channels past Cin are zero.  idx enumerates (o tile, K stage, row, chunk).
+template <typename T, int NP>
+__device__ __forceinline__ void pack_conv_chunk(const T* __restrict__ w,
+                                                uint8_t* __restrict__ pack, int Cout, int Cin,
+                                                int BN, int n_chunks, size_t idx) {
+    const int n_kiters = 3 * n_chunks;
+    const int j = (int)(idx & 7);
+    size_t rest = idx >> 3;
+    const int row = (int)(rest % BN);
+    rest /= BN;
+    const int kiter = (int)(rest % n_kiters);
+    const int ot = (int)(rest / n_kiters);
+    const int tap = kiter / n_chunks, chunk = kiter % n_chunks;
+    const int o = ot * BN + row;
+    const int c0 = chunk * kBK + j * 8;
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int c = c0 + e;
+        v[e] = (o < Cout && c < Cin) ? load_f<T>(w + ((size_t)o * Cin + c) * 3 + tap) : 0.f;
+    }
+    const size_t blk = ((size_t)ot * n_kiters + kiter) * NP;
+    const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)j);
+    uint4* hi = reinterpret_cast<uint4*>(pack + (blk * BN) * 128 + off);
+    if constexpr (NP == 2) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_bf16x2(v[2 * e], v[2 * e + 1], h[e], l[e]);
+        *hi = make_uint4(h[0], h[1], h[2], h[3]);
+        uint4* lo = reinterpret_cast<uint4*>(pack + ((blk + 1) * BN) * 128 + off);
+        *lo = make_uint4(l[0], l[1], l[2], l[3]);
+    } else {
+        // bf16 input: values are already bf16, the repack is exact.
+        *hi = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                         pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+    }
 }
 
 // Warp-level merge of (count, mean, M2) triples (Chan et al.'s pairwise
@@ -228,7 +275,11 @@ __device__ __forceinline__ void gn_tile_stats(const float* bias_s, uint32_t tadd
     }
 }
 
-template <typename T, ConvEpi EPI, bool STAGED>
+// ONE_WAVE: every tile on its own CTA, all resident (cooperative launch).  The
+// kernel then also repacks the weight image (see pack_counter) and, for
+// GroupNorm, finishes the normalization (gn_fused).  A separate instantiation,
+// so the kernels of larger problems carry none of it.
+template <typename T, ConvEpi EPI, bool STAGED, bool ONE_WAVE = false>
 struct ConvProblem {
     using Params = ConvParams;
     using Tile = ConvTile;
@@ -243,7 +294,26 @@ struct ConvProblem {
         return conv_tile(p, tile);
     }
 
+    // Non-NULL: the B producer waits until every CTA has packed its share.
+    static __device__ __forceinline__ uint32_t* b_ready_counter(const Params& p) {
+        if constexpr (ONE_WAVE)
+            return p.pack_counter;
+        else
+            return nullptr;
+    }
+
     static __device__ void setup(const Params& p, uint8_t* extra, int tid, int nthr) {
+        if constexpr (ONE_WAVE) {
+            // this CTA's share of the weight image, published to the copy engine
+            constexpr int NP = sizeof(T) == 4 ? 2 : 1;
+            const size_t units = (size_t)p.n_ot * p.n_kiters * p.BN * 8;
+            for (size_t idx = (size_t)blockIdx.x * nthr + tid; idx < units;
+                 idx += (size_t)gridDim.x * nthr)
+                pack_conv_chunk<T, NP>(static_cast<const T*>(p.w_raw), p.wpack_out, p.Cout,
+                                       p.Cin, p.BN, p.n_chunks, idx);
+            fence_proxy_async_global();
+            __threadfence();
+        }
         float* ex = reinterpret_cast<float*>(extra);
         // Conv bias for every (padded) output channel, staged once per CTA so
         // the epilogue reads it from shared memory.
@@ -251,7 +321,7 @@ struct ConvProblem {
         // (32 zero floats past the last tile, so vector reads never leave the region)
         for (int o = tid; o < p.n_ot * p.BN + 32; o += nthr)
             ex[p.bias_off + o] = (bias && o < p.Cout) ? load_f<T>(bias + o) : 0.f;
-        if (EPI == ConvEpi::kGroupStats && p.fused) {
+        if constexpr (ONE_WAVE && EPI == ConvEpi::kGroupStats) {
             // one tile per CTA: its channels' gamma and beta, staged while the
             // mainloop runs (the epilogue turns them into scale and shift)
             const int obase = conv_tile(p, (int)blockIdx.x).ot * p.BN;
@@ -543,7 +613,7 @@ struct ConvProblem {
             // is uniform across the warp except t_ok (invalid rows count 0).
             for (int h = 0; h < halves; ++h)
                 if (!acquire(h)) return false;
-            if (p.fused) {
+            if constexpr (ONE_WAVE) {
                 const bool ok = gn_fused(p, extra, tl, quarter, lane, taddr, BN);
                 for (int h = 0; h < halves; ++h) release(h);
                 return ok;
@@ -819,41 +889,10 @@ struct ConvProblem {
 template <typename T, int NP>
 __global__ void pack_conv_weight_kernel(const T* __restrict__ w, uint8_t* __restrict__ pack,
                                         int Cout, int Cin, int BN, int n_ot, int n_chunks) {
-    const int n_kiters = 3 * n_chunks;
-    const size_t total = (size_t)n_ot * n_kiters * BN * 8;   // 16-byte chunks per part
+    const size_t total = (size_t)n_ot * 3 * n_chunks * BN * 8;   // 16-byte chunks per part
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (size_t)gridDim.x * blockDim.x) {
-        const int j = (int)(idx & 7);
-        size_t rest = idx >> 3;
-        const int row = (int)(rest % BN);
-        rest /= BN;
-        const int kiter = (int)(rest % n_kiters);
-        const int ot = (int)(rest / n_kiters);
-        const int tap = kiter / n_chunks, chunk = kiter % n_chunks;
-        const int o = ot * BN + row;
-        const int c0 = chunk * kBK + j * 8;
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int c = c0 + e;
-            v[e] = (o < Cout && c < Cin) ? load_f<T>(w + ((size_t)o * Cin + c) * 3 + tap) : 0.f;
-        }
-        const size_t blk = ((size_t)ot * n_kiters + kiter) * NP;
-        const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)j);
-        uint4* hi = reinterpret_cast<uint4*>(pack + (blk * BN) * 128 + off);
-        if constexpr (NP == 2) {
-            uint32_t h[4], l[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) split_bf16x2(v[2 * e], v[2 * e + 1], h[e], l[e]);
-            *hi = make_uint4(h[0], h[1], h[2], h[3]);
-            uint4* lo = reinterpret_cast<uint4*>(pack + ((blk + 1) * BN) * 128 + off);
-            *lo = make_uint4(l[0], l[1], l[2], l[3]);
-        } else {
-            // bf16 input: values are already bf16, the repack is exact.
-            *hi = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                             pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-        }
-    }
+         idx += (size_t)gridDim.x * blockDim.x)
+        pack_conv_chunk<T, NP>(w, pack, Cout, Cin, BN, n_chunks, idx);
 }
 
 // ---------------------------------------------------------------------------
@@ -1012,9 +1051,16 @@ static bool plan_conv_staged(ConvParams& p, ConvPlan& pl, int N, int Cin, int Co
 
 using namespace nrc;
 
+// The block's workspace: the packed weight image, then (256-byte aligned) the
+// counter of the in-kernel repack.
+static size_t block_counter_offset(int C, nrc_dtype dt) {
+    return (plan_conv(1, C, C, 1, dt == NRC_F32 ? 2 : 1, true).wpack_bytes + 255) &
+           ~(size_t)255;
+}
+
 extern "C" size_t nrc_prenorm_dilconv_residual_workspace_size(int C, nrc_dtype dt) {
     if (C <= 0 || (dt != NRC_F32 && dt != NRC_BF16)) return 0;
-    return plan_conv(1, C, C, 1, dt == NRC_F32 ? 2 : 1, true).wpack_bytes;
+    return block_counter_offset(C, dt) + 256;
 }
 
 namespace {
@@ -1041,8 +1087,8 @@ nrc_status block_pack(const void* conv_weight, nrc_dtype dt, int C, void* wpack,
 // packed weight image.  Arguments already validated.
 nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int L, int dilation,
                       int padding, const float* rm, const float* rv, const float* gamma,
-                      const float* beta, float bn_eps, const void* conv_bias,
-                      const uint8_t* wpack, cudaStream_t st) {
+                      const float* beta, float bn_eps, const void* conv_bias, uint8_t* wpack,
+                      const void* w_raw, uint32_t* pack_counter, cudaStream_t st) {
     const int NP = dt == NRC_F32 ? 2 : 1;
     ConvPlan pl = plan_conv(N, C, C, L, NP, true);
     if ((long long)N * pl.n_tt * pl.n_ot >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
@@ -1070,18 +1116,38 @@ nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int 
     p.bias = conv_bias;
     p.bias_off = 2 * pl.n_chunks * kBK;
     p.wpack = wpack;
+    // One wave with the staged kernel: the GEMM kernel repacks the weights
+    // (cooperative launch); otherwise the separate repack, when asked for.
+    const bool one_wave = pack_counter != nullptr && staged;
+    if (one_wave) {
+        p.w_raw = w_raw;
+        p.wpack_out = wpack;
+        p.pack_counter = pack_counter;
+        if (cudaMemsetAsync(pack_counter, 0, sizeof(uint32_t), st) != cudaSuccess)
+            return NRC_ERR_CUDA;
+        pl.g.coop = true;
+    } else if (pack_counter) {
+        const nrc_status s = block_pack(w_raw, dt, C, wpack, st);
+        if (s != NRC_OK) return s;
+    }
     // Residual drain overlapped at tile boundaries (whole 128-column halves).
     if (pl.g.BN % 128 == 0) {
         const int SA = 256 / (32 * NP);
         pl.g.split_h = std::min(std::min(SA, pl.g.b_stages), pl.g.num_kiters / 2);
     }
     if (dt == NRC_F32) {
+        if (one_wave)
+            return launch_gemm<ConvProblem<float, ConvEpi::kResidual, true, true>, 2>(
+                "prenorm_block_gemm", p, pl.g, st);
         if (staged)
             return launch_gemm<ConvProblem<float, ConvEpi::kResidual, true>, 2>(
                 "prenorm_block_gemm", p, pl.g, st);
         return launch_gemm<ConvProblem<float, ConvEpi::kResidual, false>, 2>(
             "prenorm_block_gemm", p, pl.g, st);
     }
+    if (one_wave)
+        return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual, true, true>, 1>(
+            "prenorm_block_gemm", p, pl.g, st);
     if (staged)
         return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual, true>, 1>(
             "prenorm_block_gemm", p, pl.g, st);
@@ -1120,10 +1186,22 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual(
     if (workspace_bytes < nrc_prenorm_dilconv_residual_workspace_size(C, dt))
         return NRC_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    // Problems of one wave (every tile on its own CTA): one launch, the GEMM
+    // kernel repacks the weights itself (this saves a launch and its gap, a
+    // large share of a short call).  A longer GEMM gains nothing from it: its
+    // first weight stages would wait for the whole grid's repack.
+    const int n_tiles = plan_conv(N, C, C, L, dt == NRC_F32 ? 2 : 1, true).g.num_tiles;
+    if (n_tiles <= device_sm_count() && device_coop_launch()) {
+        // (block_gemm packs separately if the staged kernel does not apply)
+        uint32_t* counter = reinterpret_cast<uint32_t*>(ws + block_counter_offset(C, dt));
+        return block_gemm(x, out, dt, N, C, L, dilation, padding, rm, rv, gamma, beta, bn_eps,
+                          conv_bias, ws, conv_weight, counter, st);
+    }
     const nrc_status s = block_pack(conv_weight, dt, C, workspace, st);
     if (s != NRC_OK) return s;
     return block_gemm(x, out, dt, N, C, L, dilation, padding, rm, rv, gamma, beta, bn_eps,
-                      conv_bias, static_cast<const uint8_t*>(workspace), st);
+                      conv_bias, ws, nullptr, nullptr, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -1260,7 +1338,8 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual_host(
             return NRC_ERR_CUDA;
         s = block_gemm(ws + hl.x[b], ws + hl.o[b], dt, cn, C, L, dilation, padding, par,
                        par + C, par + 2 * C, par + 3 * C, bn_eps,
-                       bias_host ? static_cast<const void*>(ws + hl.b) : nullptr, ws, st);
+                       bias_host ? static_cast<const void*>(ws + hl.b) : nullptr, ws, nullptr,
+                       nullptr, st);
         if (s != NRC_OK) return s;
         if (!ok(cudaEventRecord(hp->ev_gemm[b], st))) return NRC_ERR_CUDA;
         // copy-out
@@ -1320,7 +1399,11 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     // One wave (every tile on its own CTA, all resident): the GroupNorm is
     // finished inside the GEMM kernel behind a grid-wide barrier.
     p.fused = (pl.g.num_tiles <= device_sm_count() && device_coop_launch()) ? 1 : 0;
-    const bool staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
+    bool staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
+    if (p.fused && !staged) {           // the one-wave kernel is the staged one
+        p.fused = 0;
+        staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
+    }
     p.N = N;
     p.Cin = C_in;
     p.Cout = C_out;
@@ -1338,16 +1421,20 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     p.partials = reinterpret_cast<float2*>(ws + gn_partials_offset(pl));
     p.G = num_groups;
     p.cpg = cpg;
-    const size_t units = pl.wpack_bytes / 16 / 2;
-    {
+    if (!p.fused) {
+        const size_t units = pl.wpack_bytes / 16 / 2;
         TraceScope ts("pack_conv_weight", st);
         pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
             conv_weight, ws, C_out, C_in, pl.g.BN, pl.n_ot, pl.n_chunks);
+        if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
     }
-    if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
     if (p.fused) {
+        // one launch: the GEMM kernel also repacks the weights
         uint8_t* part = ws + gn_partials_offset(pl);
         p.grid_counter = reinterpret_cast<uint32_t*>(part);
+        p.pack_counter = reinterpret_cast<uint32_t*>(part + 4);
+        p.w_raw = conv_weight;
+        p.wpack_out = ws;
         p.tile_stats = reinterpret_cast<float4*>(part + 256);
         p.gn_gamma = gn_gamma;
         p.gn_beta = gn_beta;
@@ -1355,15 +1442,17 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
         p.status = device_status_ptr();
         p.timeout_ns = wait_timeout_ns();
         if (p.status == nullptr) return NRC_ERR_CUDA;
-        if (cudaMemsetAsync(p.grid_counter, 0, sizeof(uint32_t), st) != cudaSuccess)
+        if (cudaMemsetAsync(p.grid_counter, 0, 2 * sizeof(uint32_t), st) != cudaSuccess)
             return NRC_ERR_CUDA;
         pl.g.coop = true;
     }
     nrc_status s =
-        staged ? launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true>, 2>("conv_gn_gemm",
-                                                                               p, pl.g, st)
-               : launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, false>, 2>(
-                     "conv_gn_gemm", p, pl.g, st);
+        p.fused ? launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true, true>, 2>(
+                      "conv_gn_gemm", p, pl.g, st)
+        : staged ? launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true>, 2>("conv_gn_gemm",
+                                                                                 p, pl.g, st)
+                 : launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, false>, 2>(
+                       "conv_gn_gemm", p, pl.g, st);
     if (s != NRC_OK || p.fused) return s;
     {
         TraceScope ts("groupnorm_finalize_normalize", st);

@@ -53,6 +53,8 @@ struct LinearProblem {
         return Tile{tile / p.n_bt, tile % p.n_bt};
     }
 
+    static __device__ __forceinline__ uint32_t* b_ready_counter(const Params&) { return nullptr; }
+
     static __device__ void setup(const Params&, uint8_t*, int, int) {}
 
     static __device__ __forceinline__ void load_a(const Params& p, const Tile& tl, int kiter,

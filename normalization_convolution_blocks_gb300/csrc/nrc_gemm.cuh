@@ -60,7 +60,7 @@ constexpr uint32_t kTmemARing = 256;           // first column of the A ring
 
 enum WaitSite : int {
     kSiteBEmpty = 1, kSiteAEmpty = 2, kSiteAccEmpty = 3, kSiteFullA = 4, kSiteFullB = 5,
-    kSiteAccFull = 6, kSiteFullX = 7, kSiteEmptyX = 8, kSiteGridBarrier = 9
+    kSiteAccFull = 6, kSiteFullX = 7, kSiteEmptyX = 8, kSiteGridBarrier = 9, kSiteBImage = 10
 };
 
 struct GemmCfg {
@@ -105,6 +105,10 @@ __device__ __forceinline__ void split_store_a(uint32_t taddr_hi, const float (&v
 //   static __device__ void setup(const Params&, uint8_t* extra, int tid, int nthreads)
 //        -> stages the block's parameters in the extra bytes; run by warps 1-13
 //           (tid in [0, nthreads)) while the copy warps issue the first stages
+//   static __device__ uint32_t* b_ready_counter(const Params&)
+//        -> non-NULL when setup also writes part of the B image in global memory:
+//           each CTA then arrives on it once setup is done and the B producer
+//           waits (bounded) until all gridDim.x have (all CTAs resident)
 //   static __device__ void load_a(const Params&, const Tile&, int kiter, int row, int k0,
 //                                 float (&v)[32])
 //        -> issues the loads of the raw values A[row][kiter*64 + k0 .. +32)
@@ -203,6 +207,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(2, kThreads - 64);
         tc_fence_after();
         tmem_base = *tmem_slot;
+        if (threadIdx.x == 32) {
+            if (uint32_t* c = Prob::b_ready_counter(p)) {
+                __threadfence();
+                atomicAdd(c, 1u);
+            }
+        }
     }
 
     if (warp == 0) {
@@ -214,6 +224,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool armed[kMaxStages];
             for (int s = 0; s < kMaxStages; ++s) armed[s] = false;
             bool ok = true;
+            if (uint32_t* c = Prob::b_ready_counter(p)) {
+                // the B image is written by all CTAs' setup: wait for every one
+                const uint64_t t0 = globaltimer_ns();
+                while (ld_acquire_gpu(c) < gridDim.x) {
+                    if (globaltimer_ns() - t0 > cfg.timeout_ns) {
+                        record_status(cfg.status, kStatusTimeout, kSiteBImage);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+                fence_proxy_async_global();
+            }
             for (int tile = blockIdx.x; ok && tile < cfg.num_tiles; tile += gridDim.x) {
                 const Tile tl = Prob::tile_info(p, tile);
                 for (int k = 0; k < cfg.num_kiters; ++k) {

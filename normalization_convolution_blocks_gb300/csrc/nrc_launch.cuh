@@ -13,7 +13,7 @@ namespace nrc {
 struct GemmPlan {
     int BN, num_tiles, num_kiters, b_stages, x_depth;
     int split_h;            // accumulator handed over in column halves, H stages (0: whole)
-    bool coop;              // cooperative launch, one CTA per tile (all resident at once)
+    bool coop;              // cooperative launch: all CTAs resident at once (grid-wide waits)
     uint32_t b_stage_bytes, x_box_bytes, extra_bytes, smem_bytes;
 };
 
@@ -86,11 +86,11 @@ inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
     if (cfg.status == nullptr) return NRC_ERR_CUDA;
     // Each CTA allocates all 512 TMEM columns, so one CTA per SM.
     if (pl.coop) {
-        // every tile on its own CTA, all resident (the kernel synchronises the
-        // grid): the driver refuses the launch if they cannot be
-        if (pl.num_tiles > device_sm_count() || !device_coop_launch()) return NRC_ERR_UNSUPPORTED;
+        // all CTAs resident (they wait on one another): the driver refuses the
+        // launch if they cannot be
+        if (!device_coop_launch()) return NRC_ERR_UNSUPPORTED;
         cudaLaunchConfig_t lc{};
-        lc.gridDim = dim3((unsigned)pl.num_tiles);
+        lc.gridDim = dim3((unsigned)std::min(pl.num_tiles, device_sm_count()));
         lc.blockDim = dim3(kThreads);
         lc.dynamicSmemBytes = pl.smem_bytes;
         lc.stream = stream;

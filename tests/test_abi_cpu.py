@@ -49,9 +49,10 @@ def test_status_strings(lib):
 
 def test_workspace_queries(lib):
     from normalization_convolution_blocks_gb300 import api
-    # fp32 block: C=256 -> one 256-wide o tile, 12 K stages, hi+lo parts of 256 x 128 B
-    assert api.prenorm_dilconv_residual_workspace_size(256) == 12 * 2 * 256 * 128
-    assert api.prenorm_dilconv_residual_workspace_size(256, dtype=None) == 12 * 256 * 128
+    # fp32 block: C=256 -> one 256-wide o tile, 12 K stages, hi+lo parts of 256 x 128 B,
+    # then 256 bytes for the in-kernel repack's counter
+    assert api.prenorm_dilconv_residual_workspace_size(256) == 12 * 2 * 256 * 128 + 256
+    assert api.prenorm_dilconv_residual_workspace_size(256, dtype=None) == 12 * 256 * 128 + 256
     assert lib.nrc_prenorm_dilconv_residual_workspace_size(0, 0) == 0
     assert api.conv1d_groupnorm_workspace_size(16, 128, 256, 1024, 32) > 0
     assert api.linear_bn_swish_workspace_size(1024, 8192, 8192) > 2 * 1024 * 8192 * 2
