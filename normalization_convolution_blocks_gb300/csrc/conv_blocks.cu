@@ -889,6 +889,7 @@ struct ConvProblem {
 template <typename T, int NP>
 __global__ void pack_conv_weight_kernel(const T* __restrict__ w, uint8_t* __restrict__ pack,
                                         int Cout, int Cin, int BN, int n_ot, int n_chunks) {
+    griddep_launch_dependents();       // the GEMM may launch; it waits before reading B
     const size_t total = (size_t)n_ot * 3 * n_chunks * BN * 8;   // 16-byte chunks per part
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
          idx += (size_t)gridDim.x * blockDim.x)
@@ -1116,9 +1117,11 @@ nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int 
     p.bias = conv_bias;
     p.bias_off = 2 * pl.n_chunks * kBK;
     p.wpack = wpack;
-    // One wave with the staged kernel: the GEMM kernel repacks the weights
-    // (cooperative launch); otherwise the separate repack, when asked for.
-    const bool one_wave = pack_counter != nullptr && staged;
+    // w_raw given: repack it.  One wave (pack_counter given) with the staged
+    // kernel: inside the GEMM kernel (cooperative launch); otherwise by the
+    // repack kernel, with the GEMM launched behind it (it waits only to read B).
+    // w_raw NULL: wpack already holds the image.
+    const bool one_wave = w_raw != nullptr && pack_counter != nullptr && staged;
     if (one_wave) {
         p.w_raw = w_raw;
         p.wpack_out = wpack;
@@ -1126,9 +1129,10 @@ nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int 
         if (cudaMemsetAsync(pack_counter, 0, sizeof(uint32_t), st) != cudaSuccess)
             return NRC_ERR_CUDA;
         pl.g.coop = true;
-    } else if (pack_counter) {
+    } else if (w_raw) {
         const nrc_status s = block_pack(w_raw, dt, C, wpack, st);
         if (s != NRC_OK) return s;
+        pl.g.b_after_prev = true;
     }
     // Residual drain overlapped at tile boundaries (whole 128-column halves).
     if (pl.g.BN % 128 == 0) {
@@ -1198,10 +1202,9 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual(
         return block_gemm(x, out, dt, N, C, L, dilation, padding, rm, rv, gamma, beta, bn_eps,
                           conv_bias, ws, conv_weight, counter, st);
     }
-    const nrc_status s = block_pack(conv_weight, dt, C, workspace, st);
-    if (s != NRC_OK) return s;
+    // the repack, then the GEMM launched behind it (it waits only to read B)
     return block_gemm(x, out, dt, N, C, L, dilation, padding, rm, rv, gamma, beta, bn_eps,
-                      conv_bias, ws, nullptr, nullptr, st);
+                      conv_bias, ws, conv_weight, nullptr, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -1427,6 +1430,7 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
         pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
             conv_weight, ws, C_out, C_in, pl.g.BN, pl.n_ot, pl.n_chunks);
         if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
+        pl.g.b_after_prev = true;      // the GEMM launched behind the repack
     }
     if (p.fused) {
         // one launch: the GEMM kernel also repacks the weights

@@ -167,6 +167,7 @@ struct LinearProblem {
 // ---------------------------------------------------------------------------
 __global__ void pack_rows_split_kernel(const float* __restrict__ x, uint8_t* __restrict__ pack,
                                        int B, int IN, int BN, int n_bt, int n_kiters) {
+    griddep_launch_dependents();       // the GEMM may launch; it waits before reading B
     const size_t total = (size_t)n_bt * n_kiters * BN * 8;
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
          idx += (size_t)gridDim.x * blockDim.x) {
@@ -370,6 +371,7 @@ extern "C" nrc_status nrc_linear_bn_swish(
             x, ws, B, in_f, pl.g.BN, pl.n_bt, pl.g.num_kiters);
     }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
+    pl.g.b_after_prev = true;          // launched behind the x repack
     nrc_status s = staged ? launch_gemm<LinearProblem<true>, 2>("linear_gemm", p, pl.g, st)
                           : launch_gemm<LinearProblem<false>, 2>("linear_gemm", p, pl.g, st);
     if (s != NRC_OK) return s;

@@ -75,6 +75,9 @@ struct GemmCfg {
                             // each tile end (H <= both ring depths, 2H <= num_kiters)
     int* status;            // device status word
     unsigned long long timeout_ns;
+    int b_after_prev;       // B image written by the previous kernel of the stream, which
+                            // may still run (programmatic dependent launch): the B
+                            // producer waits for it (griddepcontrol.wait) first
 };
 
 // Shared-memory bookkeeping after the B stages and A-source slots: barriers
@@ -224,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool armed[kMaxStages];
             for (int s = 0; s < kMaxStages; ++s) armed[s] = false;
             bool ok = true;
+            if (cfg.b_after_prev) griddep_wait();
             if (uint32_t* c = Prob::b_ready_counter(p)) {
                 // the B image is written by all CTAs' setup: wait for every one
                 const uint64_t t0 = globaltimer_ns();

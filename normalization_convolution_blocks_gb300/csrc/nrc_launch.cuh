@@ -14,6 +14,7 @@ struct GemmPlan {
     int BN, num_tiles, num_kiters, b_stages, x_depth;
     int split_h;            // accumulator handed over in column halves, H stages (0: whole)
     bool coop;              // cooperative launch: all CTAs resident at once (grid-wide waits)
+    bool b_after_prev;      // programmatic dependent launch after the kernel writing B
     uint32_t b_stage_bytes, x_box_bytes, extra_bytes, smem_bytes;
 };
 
@@ -83,6 +84,7 @@ inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
     }
     cfg.status = device_status_ptr();
     cfg.timeout_ns = wait_timeout_ns();
+    cfg.b_after_prev = pl.b_after_prev ? 1 : 0;
     if (cfg.status == nullptr) return NRC_ERR_CUDA;
     // Each CTA allocates all 512 TMEM columns, so one CTA per SM.
     if (pl.coop) {
@@ -105,6 +107,23 @@ inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
         return cuda_status(cudaGetLastError());
     }
     const int grid = std::min(pl.num_tiles, device_sm_count());
+    if (pl.b_after_prev) {
+        // may start while the kernel writing B finishes; the B producer waits
+        cudaLaunchConfig_t lc{};
+        lc.gridDim = dim3((unsigned)grid);
+        lc.blockDim = dim3(kThreads);
+        lc.dynamicSmemBytes = pl.smem_bytes;
+        lc.stream = stream;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.attrs = at;
+        lc.numAttrs = 1;
+        TraceScope ts(name, stream);
+        const cudaError_t e = cudaLaunchKernelEx(&lc, kern, p, cfg);
+        if (e != cudaSuccess) return cuda_status(e);
+        return cuda_status(cudaGetLastError());
+    }
     {
         TraceScope ts(name, stream);
         kern<<<grid, kThreads, pl.smem_bytes, stream>>>(p, cfg);

@@ -365,6 +365,16 @@ __device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
 }
 
 // Named barrier `id` (1..15) over `count` threads (a multiple of 32) of the CTA.
+// Programmatic dependent launch: let the next kernel of the stream start
+// launching (it must griddep_wait before reading this kernel's results), and
+// wait for the previous kernel's completion and memory.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Acquire load of a global word at GPU scope (grid-wide flags and counters).
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;
