@@ -207,6 +207,8 @@ __global__ void bn_finalize_kernel(const float4* __restrict__ partials, int n_bt
                                    long long* __restrict__ nbt, float eps, float momentum,
                                    int training, const float* __restrict__ add_bias,
                                    float divide_value, float* __restrict__ colp) {
+    griddep_launch_dependents();
+    griddep_wait();                    // the GEMM's partials
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     if (training && nbt && j == 0) *nbt += 1;
     if (j >= OUT) return;
@@ -249,6 +251,7 @@ __device__ __forceinline__ float swish_f(float u) { return u / (1.0f + expf(-u))
 // 16-byte aligned, one at a time otherwise.
 __global__ void normalize_swish_kernel(float* __restrict__ out, const float* __restrict__ colp,
                                        int B, int OUT) {
+    griddep_wait();                    // y from the GEMM, the column parameters
     const int vec = (OUT % 4 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) ? 4 : 1;
     const int j = (blockIdx.x * blockDim.x + threadIdx.x) * vec;
     if (j >= OUT) return;
@@ -377,10 +380,12 @@ extern "C" nrc_status nrc_linear_bn_swish(
     if (s != NRC_OK) return s;
     {
         TraceScope ts("bn_finalize", st);
-        bn_finalize_kernel<<<ceil_div(out_f, 256), 256, 0, st>>>(
-            p.partials, pl.n_bt, B, out_f, bn_gamma, bn_beta, bn_running_mean, bn_running_var,
-            reinterpret_cast<long long*>(num_batches_tracked), bn_eps, bn_momentum, training,
-            add_bias, divide_value, colp);
+        const cudaError_t e = launch_after_prev(
+            bn_finalize_kernel, dim3(ceil_div(out_f, 256)), dim3(256), st,
+            static_cast<const float4*>(p.partials), pl.n_bt, B, out_f, bn_gamma, bn_beta,
+            bn_running_mean, bn_running_var, reinterpret_cast<long long*>(num_batches_tracked),
+            bn_eps, bn_momentum, training, add_bias, divide_value, colp);
+        if (e != cudaSuccess) return cuda_status(e);
     }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
     {
@@ -390,7 +395,10 @@ extern "C" nrc_status nrc_linear_bn_swish(
         const int vec = (out_f % 4 == 0 && aligned(out, 16)) ? 4 : 1;
         const int gx = ceil_div(ceil_div(out_f, vec), 256);
         const int gy = std::max(1, std::min(B, device_sm_count() * 8 / std::max(gx, 1)));
-        normalize_swish_kernel<<<dim3(gx, gy), 256, 0, st>>>(out, colp, B, out_f);
+        const cudaError_t e = launch_after_prev(normalize_swish_kernel, dim3(gx, gy), dim3(256),
+                                                st, out, static_cast<const float*>(colp), B,
+                                                out_f);
+        if (e != cudaSuccess) return cuda_status(e);
     }
     return cuda_status(cudaGetLastError());
 }

@@ -172,6 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a kernel launched behind this one may start launching (it waits for our
+    // completion before reading our results)
+    griddep_launch_dependents();
     const int BN = cfg.BN;
     WaitCtx ctx{abort_flag, cfg.status, cfg.timeout_ns};
 

@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <utility>
 
 #include "nrc_gemm.cuh"
 #include "nrc_host.h"
@@ -129,6 +130,25 @@ inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
         kern<<<grid, kThreads, pl.smem_bytes, stream>>>(p, cfg);
     }
     return cuda_status(cudaGetLastError());
+}
+
+// Launch that may start while the previous kernel of the stream finishes
+// (programmatic dependent launch): the kernel must griddep_wait before it
+// reads that kernel's results.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_after_prev(void (*kern)(KArgs...), dim3 grid, dim3 block,
+                                     cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = 0;
+    lc.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kern, std::forward<Args>(args)...);
 }
 
 inline int elementwise_grid(size_t units, int per_sm = 8) {
