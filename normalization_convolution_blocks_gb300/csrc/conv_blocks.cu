@@ -20,6 +20,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "nrc_launch.cuh"
 
@@ -1220,6 +1221,32 @@ struct HostLayout {
     size_t par, w, b, x[2], o[2], total;
 };
 
+// The host entry's chunk sizes (samples): ramp-up chunk_n/4, chunk_n/2, then
+// chunk_n, then ramp-down chunk_n/2, chunk_n/4 (each at least 1; the last
+// middle chunk shorter if N asks).  chunk_n <= N.
+std::vector<int> host_chunk_sizes(int N, int chunk_n) {
+    const int r1 = std::max(1, chunk_n / 4), r2 = std::max(1, chunk_n / 2);
+    std::vector<int> sizes;
+    int rem = N;
+    auto push = [&](int t) {
+        if (t > 0) {
+            sizes.push_back(t);
+            rem -= t;
+        }
+    };
+    push(std::min(r1, rem));
+    push(std::min(r2, rem));
+    const int tail = std::min(rem, r1 + r2);
+    while (rem > tail) push(std::min(chunk_n, rem - tail));
+    if (tail > r1) {
+        push(tail - r1);
+        push(r1);
+    } else {
+        push(tail);
+    }
+    return sizes;
+}
+
 HostLayout host_layout(int N, int C, int L, nrc_dtype dt, int chunk_n) {
     const size_t es = dt == NRC_F32 ? 4 : 2;
     auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
@@ -1324,10 +1351,15 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual_host(
         return NRC_ERR_CUDA;
     const uint8_t* xh = static_cast<const uint8_t*>(x_host);
     uint8_t* oh = static_cast<uint8_t*>(out_host);
-    const int n_chunks = (N + chunk_n - 1) / chunk_n;
-    for (int j = 0; j < n_chunks; ++j) {
+    // Chunk sizes ramp up and down (chunk_n/4, chunk_n/2, chunk_n ..., chunk_n/2,
+    // chunk_n/4): the first copy-in and the last copy-out overlap nothing, so
+    // they are kept short.
+    const std::vector<int> sizes = host_chunk_sizes(N, chunk_n);
+    const int n_chunks = (int)sizes.size();
+    int n0 = 0;
+    for (int j = 0; j < n_chunks; n0 += sizes[j], ++j) {
         const int b = j & 1;
-        const int n0 = j * chunk_n, cn = std::min(chunk_n, N - n0);
+        const int cn = sizes[j];
         const size_t bytes = (size_t)cn * sample;
         // copy-in: buffer b is free once the GEMM of chunk j-2 has read it
         if (j >= 2 && !ok(cudaStreamWaitEvent(hp->in, hp->ev_gemm[b], 0))) return NRC_ERR_CUDA;
