@@ -130,7 +130,7 @@ def test_full_workload_fp32_sampled_rows():
     assert_f32(got[rn, ro], ref, "full workload rows")
 
 
-@pytest.mark.parametrize("C,d", [(256, 1), (512, 512)])
+@pytest.mark.parametrize("C,d", [(C, d) for C in (256, 512) for d in (1, 8, 128, 512)])
 def test_full_bf16_workload_sampled_rows(C, d):
     dev = need_gpu()
     inp = syn.WORKLOADS[f"prenorm_block_bf16_C{C}_d{d}"].make(seed=0)
