@@ -1124,13 +1124,26 @@ nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int 
     // w_raw NULL: wpack already holds the image.
     const bool one_wave = w_raw != nullptr && pack_counter != nullptr && staged;
     if (one_wave) {
-        p.w_raw = w_raw;
-        p.wpack_out = wpack;
-        p.pack_counter = pack_counter;
+        ConvParams p1 = p;
+        GemmPlan g1 = pl.g;
+        p1.w_raw = w_raw;
+        p1.wpack_out = wpack;
+        p1.pack_counter = pack_counter;
         if (cudaMemsetAsync(pack_counter, 0, sizeof(uint32_t), st) != cudaSuccess)
             return NRC_ERR_CUDA;
-        pl.g.coop = true;
-    } else if (w_raw) {
+        g1.coop = true;
+        if (g1.BN % 128 == 0)
+            g1.split_h = std::min(std::min(256 / (32 * NP), g1.b_stages), g1.num_kiters / 2);
+        const nrc_status s =
+            dt == NRC_F32
+                ? launch_gemm<ConvProblem<float, ConvEpi::kResidual, true, true>, 2>(
+                      "prenorm_block_gemm", p1, g1, st)
+                : launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual, true, true>, 1>(
+                      "prenorm_block_gemm", p1, g1, st);
+        // refused (the CTAs cannot all be resident now): the two-launch path
+        if (s != NRC_ERR_UNSUPPORTED) return s;
+    }
+    if (w_raw) {
         const nrc_status s = block_pack(w_raw, dt, C, wpack, st);
         if (s != NRC_OK) return s;
         pl.g.b_after_prev = true;
@@ -1141,18 +1154,12 @@ nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int 
         pl.g.split_h = std::min(std::min(SA, pl.g.b_stages), pl.g.num_kiters / 2);
     }
     if (dt == NRC_F32) {
-        if (one_wave)
-            return launch_gemm<ConvProblem<float, ConvEpi::kResidual, true, true>, 2>(
-                "prenorm_block_gemm", p, pl.g, st);
         if (staged)
             return launch_gemm<ConvProblem<float, ConvEpi::kResidual, true>, 2>(
                 "prenorm_block_gemm", p, pl.g, st);
         return launch_gemm<ConvProblem<float, ConvEpi::kResidual, false>, 2>(
             "prenorm_block_gemm", p, pl.g, st);
     }
-    if (one_wave)
-        return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual, true, true>, 1>(
-            "prenorm_block_gemm", p, pl.g, st);
     if (staged)
         return launch_gemm<ConvProblem<__nv_bfloat16, ConvEpi::kResidual, true>, 1>(
             "prenorm_block_gemm", p, pl.g, st);
@@ -1456,7 +1463,34 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     p.partials = reinterpret_cast<float2*>(ws + gn_partials_offset(pl));
     p.G = num_groups;
     p.cpg = cpg;
-    if (!p.fused) {
+    if (p.fused) {
+        // one launch: the GEMM kernel also repacks the weights
+        ConvParams p1 = p;
+        GemmPlan g1 = pl.g;
+        uint8_t* part = ws + gn_partials_offset(pl);
+        p1.grid_counter = reinterpret_cast<uint32_t*>(part);
+        p1.pack_counter = reinterpret_cast<uint32_t*>(part + 4);
+        p1.w_raw = conv_weight;
+        p1.wpack_out = ws;
+        p1.tile_stats = reinterpret_cast<float4*>(part + 256);
+        p1.gn_gamma = gn_gamma;
+        p1.gn_beta = gn_beta;
+        p1.gn_eps = eps;
+        p1.status = device_status_ptr();
+        p1.timeout_ns = wait_timeout_ns();
+        if (p1.status == nullptr) return NRC_ERR_CUDA;
+        if (cudaMemsetAsync(p1.grid_counter, 0, 2 * sizeof(uint32_t), st) != cudaSuccess)
+            return NRC_ERR_CUDA;
+        g1.coop = true;
+        const nrc_status s1 = launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true, true>, 2>(
+            "conv_gn_gemm", p1, g1, st);
+        if (s1 != NRC_ERR_UNSUPPORTED) return s1;
+        // refused (the CTAs cannot all be resident now): the two-kernel path,
+        // planned without the fused epilogue's shared memory
+        p.fused = 0;
+        staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
+    }
+    {
         const size_t units = pl.wpack_bytes / 16 / 2;
         TraceScope ts("pack_conv_weight", st);
         pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
@@ -1464,32 +1498,12 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
         if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
         pl.g.b_after_prev = true;      // the GEMM launched behind the repack
     }
-    if (p.fused) {
-        // one launch: the GEMM kernel also repacks the weights
-        uint8_t* part = ws + gn_partials_offset(pl);
-        p.grid_counter = reinterpret_cast<uint32_t*>(part);
-        p.pack_counter = reinterpret_cast<uint32_t*>(part + 4);
-        p.w_raw = conv_weight;
-        p.wpack_out = ws;
-        p.tile_stats = reinterpret_cast<float4*>(part + 256);
-        p.gn_gamma = gn_gamma;
-        p.gn_beta = gn_beta;
-        p.gn_eps = eps;
-        p.status = device_status_ptr();
-        p.timeout_ns = wait_timeout_ns();
-        if (p.status == nullptr) return NRC_ERR_CUDA;
-        if (cudaMemsetAsync(p.grid_counter, 0, 2 * sizeof(uint32_t), st) != cudaSuccess)
-            return NRC_ERR_CUDA;
-        pl.g.coop = true;
-    }
     nrc_status s =
-        p.fused ? launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true, true>, 2>(
-                      "conv_gn_gemm", p, pl.g, st)
-        : staged ? launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true>, 2>("conv_gn_gemm",
-                                                                                 p, pl.g, st)
-                 : launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, false>, 2>(
-                       "conv_gn_gemm", p, pl.g, st);
-    if (s != NRC_OK || p.fused) return s;
+        staged ? launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true>, 2>("conv_gn_gemm",
+                                                                               p, pl.g, st)
+               : launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, false>, 2>(
+                     "conv_gn_gemm", p, pl.g, st);
+    if (s != NRC_OK) return s;
     {
         TraceScope ts("groupnorm_finalize_normalize", st);
         groupnorm_finalize_normalize_kernel<<<N * num_groups, 256, 0, st>>>(

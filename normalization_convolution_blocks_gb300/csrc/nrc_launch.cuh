@@ -104,6 +104,12 @@ inline nrc_status launch_gemm(const char* name, const typename Prob::Params& p,
         lc.numAttrs = 1;
         TraceScope ts(name, stream);
         const cudaError_t e = cudaLaunchKernelEx(&lc, kern, p, cfg);
+        if (e == cudaErrorCooperativeLaunchTooLarge) {
+            // not all CTAs can be resident now (the GPU is shared): the caller
+            // takes its non-cooperative path
+            (void)cudaGetLastError();
+            return NRC_ERR_UNSUPPORTED;
+        }
         if (e != cudaSuccess) return cuda_status(e);
         return cuda_status(cudaGetLastError());
     }
