@@ -13,7 +13,12 @@
 // start rounded down to 16 bytes) is gathered as one TMA box, out-of-range rows
 // filled by the copy itself; otherwise the prologue warps load x directly.
 // The B operand (weights) is repacked once per call into the exact
-// shared-memory image the MMA reads.
+// shared-memory image the MMA reads: by a repack kernel that the GEMM is
+// launched behind (programmatic dependent launch), or, when every tile has its
+// own resident CTA (one wave, cooperative launch), inside the GEMM kernel.
+// Conv + GroupNorm in one wave also finishes the normalization inside the
+// GEMM kernel (statistics exchanged behind a grid-wide barrier); larger
+// problems run a finalize kernel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -71,7 +76,8 @@ struct ConvParams {
     float2* partials;       // [((n*G + g) * n_tt + tt) * 128 + row] = (mean, M2) of the
                             // row's cpg values (count cpg, or 0 for rows past L)
     int G, cpg;
-    // conv + GroupNorm in one wave (fused): every tile on its own resident CTA
+    // conv + GroupNorm in one wave (fused): every tile on its own resident CTA;
+    // the host's planning flag (the kernel variant is ConvProblem's ONE_WAVE)
     int fused;
     uint32_t* grid_counter;  // zeroed before the launch; one arrival per CTA
     float4* tile_stats;      // [(n*G + g) * n_tt + tt] = (count, mean, M2, 0) of a tile's group

@@ -14,7 +14,9 @@
 //
 // Launches per call: pack x -> GEMM (y + per-tile column statistics) ->
 // finalize (batch mean/var, running-stat update) -> normalize + bias +
-// divide + Swish in place.
+// divide + Swish in place.  Each of the last three is launched behind the one
+// before it (programmatic dependent launch) and waits for it before reading
+// its results.
 #include <cuda_runtime.h>
 
 #include <algorithm>

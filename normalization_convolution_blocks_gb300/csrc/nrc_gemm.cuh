@@ -27,6 +27,12 @@
 // v = hi + lo split in bf16): products exact to ~2^-16 relative, accumulated in
 // fp32.  bf16 storage runs one.
 //
+// Start-up: the copy warps (0, 14) issue the first stages at once while warps
+// 1-13 stage the block's parameters and allocate TMEM.  A kernel launched
+// behind the one writing its B image (programmatic dependent launch) waits for
+// it in the B producer only; a problem that writes its B image in its own
+// setup (one wave, cooperative launch) has the B producer wait for all CTAs.
+//
 // Warp roles (480 threads):
 //   warp 0      B producer: one thread issues the bulk copies
 //   warp 1      allocates all 512 TMEM columns; one thread issues the MMAs
