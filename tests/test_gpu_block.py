@@ -206,3 +206,36 @@ def test_bf16_views_at_odd_offsets(which):
                                        out=out)
     assert api.query_status() == api.NRC_OK
     assert_bf16(got.double().cpu().numpy(), _oracle(inp), f"bf16 {which} at +2 bytes")
+
+
+@pytest.mark.parametrize("N,C,L,d", [
+    (4, 256, 4096, 128),    # 128 tiles: one wave, the repack inside the GEMM kernel
+    (8, 256, 4096, 128),    # 256 tiles: repack kernel, GEMM launched behind it
+])
+def test_back_to_back_calls_with_alternating_weights(N, C, L, d):
+    """Calls queued back to back on one stream with different weights each time:
+    a call's repack must not overwrite the image the previous GEMM still reads,
+    and a GEMM must not read a half-written image.  Each result must equal the
+    same call run on its own."""
+    dev = need_gpu()
+    from normalization_convolution_blocks_gb300 import api
+    inp = syn.prenorm_block_inputs(N, C, L, d, seed=91)
+    w2 = torch.flip(inp.weight, dims=[0]).contiguous()
+    args = [to(dev, t) for t in (inp.x, inp.running_mean, inp.running_var, inp.gamma,
+                                 inp.beta)]
+    ws = [to(dev, inp.weight), to(dev, w2)]
+    bias = to(dev, inp.bias)
+    ref = []
+    for w in ws:
+        ref.append(api.prenorm_dilconv_residual(*args, inp.eps, w, bias, inp.dilation).clone())
+        torch.cuda.synchronize()
+    outs = [torch.empty_like(args[0]) for _ in range(6)]
+    workspace = torch.empty(api.prenorm_dilconv_residual_workspace_size(C), dtype=torch.uint8,
+                            device=dev)
+    for i, o in enumerate(outs):           # one stream, shared workspace, no syncs
+        api.prenorm_dilconv_residual(*args, inp.eps, ws[i % 2], bias, inp.dilation, out=o,
+                                     workspace=workspace)
+    torch.cuda.synchronize()
+    assert api.query_status() == api.NRC_OK
+    for i, o in enumerate(outs):
+        assert torch.equal(o, ref[i % 2]), f"call {i}"

@@ -101,3 +101,31 @@ def test_full_workload_sampled_columns():
     assert_f32(out[:, cols], r_out, "full workload columns")
     assert np.abs(rm[cols] - r_rm[cols]).max() < RUNNING_STAT_ABS
     assert np.abs(rv[cols] - r_rv[cols]).max() < RUNNING_STAT_ABS
+
+
+def test_back_to_back_calls_with_alternating_inputs():
+    """Calls queued back to back on one stream with different x each time (the
+    x repack, the GEMM launched behind it, then the chained finalize and
+    normalize): each result must equal the same call run on its own."""
+    dev = need_gpu()
+    from normalization_convolution_blocks_gb300 import api
+    li = syn.linear_bn_swish_inputs(512, 1024, 4096, seed=13, random_affine=True)
+    xs = [to(dev, li.x), to(dev, torch.flip(li.x, dims=[0]).contiguous())]
+    w, lb, g, b, ab = (to(dev, t) for t in (li.weight, li.lin_bias, li.gamma, li.beta,
+                                            li.add_bias))
+
+    def call(x, out=None):
+        rm, rv = to(dev, li.running_mean).clone(), to(dev, li.running_var).clone()
+        return api.linear_bn_swish(x, w, lb, g, b, rm, rv, ab, li.divide_value, li.eps,
+                                   li.momentum, True, None, out=out)
+    ref = []
+    for x in xs:
+        ref.append(call(x).clone())
+        torch.cuda.synchronize()
+    outs = [torch.empty_like(ref[0]) for _ in range(6)]
+    for i, o in enumerate(outs):
+        call(xs[i % 2], out=o)
+    torch.cuda.synchronize()
+    assert api.query_status() == api.NRC_OK
+    for i, o in enumerate(outs):
+        assert torch.equal(o, ref[i % 2]), f"call {i}"
