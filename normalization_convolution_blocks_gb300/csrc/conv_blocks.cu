@@ -618,13 +618,17 @@ struct ConvProblem {
             // M2), folded into the group's running triple with Chan's update,
             // and merged across the warp when the group ends.  Every test below
             // is uniform across the warp except t_ok (invalid rows count 0).
-            for (int h = 0; h < halves; ++h)
-                if (!acquire(h)) return false;
+            bool acquired = true;
+            for (int h = 0; h < halves && acquired; ++h) acquired = acquire(h);
             if constexpr (ONE_WAVE) {
+                // gn_fused meets at named barrier 1: the four warps decide
+                // together (a warp whose wait gave up would never arrive)
+                if (!named_bar_and(1, 128, acquired)) return false;
                 const bool ok = gn_fused(p, extra, tl, quarter, lane, taddr, BN);
                 for (int h = 0; h < halves; ++h) release(h);
                 return ok;
             }
+            if (!acquired) return false;
             const int ovalid = p.Cout - obase;
             float cnt = 0.f, mean = 0.f, m2 = 0.f;
             const float tw = t_ok ? 1.f : 0.f;
