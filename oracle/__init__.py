@@ -7,7 +7,9 @@ shares no code with it: the arithmetic lives in ``oracle.c`` (plain C, fp64),
 written from the problem definitions on the three PopcornBench pages:
 
 * "Kimi-K2.6 l2_p12" -- pre-norm residual block (problem statement at the top
-  of the page): out = x + Conv1d(ReLU(BatchNorm1d_eval(x))), k=3, pad=dil.
+  of the page): out = x + Conv1d(ReLU(BatchNorm1d_eval(x))), k=3, pad=dil;
+  its correctness discussion of batch against running statistics gives the
+  training-mode variant.
 * "FW-GLM-5-1 l2_p35" -- Conv1d(k=3, pad=1, no bias) + GroupNorm (problem
   analysis at the top of the page, and the normalisation kernel's formula).
 * "Kimi-K2.6 l2_p97" -- Linear + BatchNorm1d (training) + bias + divide +
@@ -67,7 +69,10 @@ def _load():
             lib.oracle_linear_bn_swish_cols.argtypes = [p, i, i, i, p, p, p, p, p, p,
                                                         d, d, i, d, d, p, i, p, p, i]
             lib.oracle_conv1d_out_len.argtypes = [i, i, i, i, i]
+            lib.oracle_prenorm_block_train.argtypes = [p, i, i, i, i, i, i, p, p, p, p, d,
+                                                       d, p, p, p, p, i, p, p, p, i]
             for f in (lib.oracle_prenorm_block, lib.oracle_prenorm_block_rows,
+                      lib.oracle_prenorm_block_train,
                       lib.oracle_conv_groupnorm, lib.oracle_conv_groupnorm_groups,
                       lib.oracle_linear_bn_swish_cols, lib.oracle_conv1d_out_len,
                       lib.oracle_max_threads):
@@ -134,6 +139,40 @@ def prenorm_block_rows(x, rm, rv, gamma, beta, eps, w, bias, dilation, rows_n, r
                                            _ptr(ro), len(rn), _ptr(out), nthreads)
     _check(rc, "prenorm_block_rows")
     return out
+
+
+def prenorm_block_train(x, running_mean, running_var, gamma, beta, eps, momentum, w, bias,
+                        dilation, rows_n=None, rows_o=None, padding=None, nthreads=0):
+    """The block with BatchNorm1d in training mode (batch mean and biased
+    variance over (N, L) per channel; running buffers updated with the
+    unbiased variance).
+
+    Returns (out, running_mean', running_var', batch_mean, batch_var): out is
+    (N, C, L), or (R, L) for the rows (rows_n[r], rows_o[r]); the running
+    statistics come back as updated float64 copies (None stays None)."""
+    x, gamma, beta, w, bias = map(_f64, (x, gamma, beta, w, bias))
+    rm = _f64(running_mean).copy() if running_mean is not None else None
+    rv = _f64(running_var).copy() if running_var is not None else None
+    N, C, L = x.shape
+    K = w.shape[2]
+    padding = dilation if padding is None else padding
+    if rows_n is None:
+        rn = ro = None
+        out = np.empty_like(x)
+        nrows = 0
+    else:
+        rn = np.ascontiguousarray(rows_n, dtype=np.int32)
+        ro = np.ascontiguousarray(rows_o, dtype=np.int32)
+        nrows = len(rn)
+        out = np.empty((nrows, L), dtype=np.float64)
+    bm = np.empty(C, dtype=np.float64)
+    bv = np.empty(C, dtype=np.float64)
+    rc = _load().oracle_prenorm_block_train(
+        _ptr(x), N, C, L, K, dilation, padding, _ptr(rm), _ptr(rv), _ptr(gamma), _ptr(beta),
+        float(eps), float(momentum), _ptr(w), _ptr(bias), _ptr(rn), _ptr(ro), nrows, _ptr(out),
+        _ptr(bm), _ptr(bv), nthreads)
+    _check(rc, "prenorm_block_train")
+    return out, rm, rv, bm, bv
 
 
 def conv_groupnorm(x, w, bias, num_groups, gamma, beta, eps, stride=1, padding=1,

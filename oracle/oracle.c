@@ -141,6 +141,87 @@ int oracle_prenorm_block(const double *x, double *out, int N, int C, int L, int 
 }
 
 /* ------------------------------------------------------------------------
+ * [P1] The same block with BatchNorm1d in training mode.  The page's
+ * correctness discussion sets batch statistics against running statistics:
+ * in training mode channel c is normalized with the mean and the biased
+ * variance of x[:, c, :] over all N*L values, and the running buffers move
+ * toward the batch values ([P3] states the rule and the update, with the
+ * unbiased variance, for the BatchNorm1d after its Linear).
+ *
+ *   mu[c]  = sum_{n,s} x[n,c,s] / (N*L)
+ *   var[c] = sum_{n,s} (x[n,c,s] - mu[c])^2 / (N*L)            (second pass)
+ *   running_mean[c] <- (1 - momentum)*running_mean[c] + momentum*mu[c]
+ *   running_var[c]  <- (1 - momentum)*running_var[c]
+ *                      + momentum*var[c]*(N*L)/(N*L - 1)
+ *   out = the eval-mode block above with mu, var in place of the running
+ *         statistics (the running buffers' old values are not used).
+ *
+ * batch_mean and batch_var (C each) receive mu and var.  running_mean and
+ * running_var may be NULL (no update).  rows_n == NULL computes every row
+ * (out_rows is then (N, C, L)); otherwise the nrows rows (rows_n[r], rows_o[r]).
+ * ------------------------------------------------------------------------ */
+int oracle_prenorm_block_train(const double *x, int N, int C, int L, int K,
+                               int dilation, int padding,
+                               double *running_mean, double *running_var,
+                               const double *gamma, const double *beta, double eps,
+                               double momentum, const double *w, const double *bias,
+                               const int *rows_n, const int *rows_o, int nrows,
+                               double *out_rows, double *batch_mean, double *batch_var,
+                               int nthreads)
+{
+    if (N <= 0 || C <= 0 || L <= 0 || K <= 0 || dilation <= 0 || padding < 0)
+        return -1;
+    if (L + 2 * padding - dilation * (K - 1) != L) return -2;
+    const double cnt = (double)N * (double)L;
+    if (cnt < 2.0) return -4;                   /* the unbiased variance needs N*L-1 */
+    if (!batch_mean || !batch_var) return -5;
+    if (rows_n)
+        for (int r = 0; r < nrows; ++r)
+            if (rows_n[r] < 0 || rows_n[r] >= N || rows_o[r] < 0 || rows_o[r] >= C)
+                return -3;
+    set_threads(nthreads);
+
+    #pragma omp parallel for schedule(static)
+    for (int c = 0; c < C; ++c) {
+        double s = 0.0;
+        for (int n = 0; n < N; ++n) {
+            const double *xc = x + ((size_t)n * C + c) * L;
+            for (int t = 0; t < L; ++t) s += xc[t];
+        }
+        const double mu = s / cnt;
+        double ss = 0.0;
+        for (int n = 0; n < N; ++n) {
+            const double *xc = x + ((size_t)n * C + c) * L;
+            for (int t = 0; t < L; ++t) {
+                const double d = xc[t] - mu;
+                ss += d * d;
+            }
+        }
+        const double var = ss / cnt;
+        batch_mean[c] = mu;
+        batch_var[c] = var;
+        if (running_mean)
+            running_mean[c] = (1.0 - momentum) * running_mean[c] + momentum * mu;
+        if (running_var)
+            running_var[c] = (1.0 - momentum) * running_var[c] +
+                             momentum * var * cnt / (cnt - 1.0);
+    }
+
+    if (!rows_n) {
+        #pragma omp parallel for schedule(dynamic)
+        for (int nc = 0; nc < N * C; ++nc)
+            block_row(x, C, L, K, dilation, padding, batch_mean, batch_var, gamma, beta, eps,
+                      w, bias, nc / C, nc % C, out_rows + (size_t)nc * L);
+    } else {
+        #pragma omp parallel for schedule(dynamic)
+        for (int r = 0; r < nrows; ++r)
+            block_row(x, C, L, K, dilation, padding, batch_mean, batch_var, gamma, beta, eps,
+                      w, bias, rows_n[r], rows_o[r], out_rows + (size_t)r * L);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
  * [P2] Conv1d followed by GroupNorm.
  *
  *   T_out = floor((T + 2*padding - dilation*(K-1) - 1)/stride) + 1

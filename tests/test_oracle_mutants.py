@@ -35,6 +35,14 @@ MUTANTS = {
     "divide dropped": ("double u = (v + add_bias) / divide_value;", "double u = (v + add_bias);"),
     "sigmoid sign": ("return 1.0 / (1.0 + exp(-u));", "return 1.0 / (1.0 + exp(u));"),
     "bn train uses running stats": ("mu = s / B;", "mu = running_mean ? running_mean[j] : s / B;"),
+    "block train: running var biased": ("momentum * var * cnt / (cnt - 1.0);", "momentum * var;"),
+    "block train: unbiased var normalizes": ("const double var = ss / cnt;",
+                                             "const double var = ss / (cnt - 1.0);"),
+    "block train: first sample only": ("for (int t = 0; t < L; ++t) s += xc[t];",
+                                       "for (int t = 0; t < L; ++t) s += n == 0 ? N * xc[t] : 0.0;"),
+    "block train: momentum swapped": (
+        "running_mean[c] = (1.0 - momentum) * running_mean[c] + momentum * mu;",
+        "running_mean[c] = momentum * running_mean[c] + (1.0 - momentum) * mu;"),
 }
 
 
@@ -51,7 +59,8 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                     str(mutant_c), "-lm"], check=True)
     env = dict(os.environ, ORACLE_LIB_OVERRIDE=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        "tests/test_oracle_block.py", "tests/test_oracle_gn.py",
+                        "tests/test_oracle_block.py", "tests/test_oracle_block_train.py",
+                        "tests/test_oracle_gn.py",
                         "tests/test_oracle_linear.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"mutant '{name}' survived the pins:\n{r.stdout[-2000:]}"
