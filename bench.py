@@ -54,10 +54,14 @@ NCU_TRAFFIC = {
                           "profile": "profiles/gemm_prenorm_block_f32_N32_C256_L4096_d128.md"},
     "linear_bn_swish_f32": {"bytes": 358642688, "src_hash": "779716fe7b7bbb47",
                             "profile": "profiles/gemm_linear_bn_swish_f32_B1024_IN8192_OUT8192.md"},
+    "prenorm_block_train_f32": {"bytes": 221418240, "src_hash": "41640fe1382ffc87",
+                                "profile": "profiles/prenorm_block_train_f32_N32_C256_L4096_d128.md"},
     "conv1d_groupnorm_f32": {"bytes": 8901120, "src_hash": "41640fe1382ffc87",
                              "profile": "profiles/gemm_conv1d_groupnorm_f32_N16_C128_256_T1024_G32.md"},
 }
-KERNEL_TU = {"block": "conv_blocks.cu", "conv_gn": "conv_blocks.cu", "linear": "linear_bn_swish.cu"}
+KERNEL_TU = {"block": "conv_blocks.cu", "block_train": "conv_blocks.cu",
+             "conv_gn": "conv_blocks.cu", "linear": "linear_bn_swish.cu"}
+TRAIN_MOMENTUM = 0.1
 
 
 def kernel_source_hash(workload: str) -> str:
@@ -91,13 +95,17 @@ def workload_info(name):
     from normalization_convolution_blocks_gb300 import synthetic as syn
     wl = syn.WORKLOADS[name]
     p = wl.params
-    if wl.kind == "block":
+    if wl.kind in ("block", "block_train"):
         esz = 2 if p.get("dtype") == "bf16" else 4
         N, C, L = p["N"], p["C"], p["L"]
         flops = 2.0 * N * L * C * C * 3
         min_bytes = esz * (2 * N * C * L + 3 * C * C + C) + 4 * 4 * C
         cfg = dict(workload=name, N=N, C=C, L=L, kernel_size=3, dilation=p["dilation"],
                    padding=p["dilation"], storage=p.get("dtype", "f32"))
+        if wl.kind == "block_train":
+            # min_bytes stays the GEMM's own; the statistics pass before it reads
+            # x once more (reported on its own, see stats_kernel)
+            cfg.update(bn="training", momentum=TRAIN_MOMENTUM)
         dtype = "bf16" if esz == 2 else "f32"
         main = "prenorm_block_gemm"
     elif wl.kind == "conv_gn":
@@ -285,6 +293,21 @@ def make_call(name, dev, host=False):
             return api.prenorm_dilconv_residual(x, rm, rv, g, b, inp.eps, w, bias,
                                                 inp.dilation, out=out, workspace=ws)
         out_shape = (x.shape, x.dtype)
+    elif wl.kind == "block_train":
+        x, g, b, w, bias = map(place, (inp.x, inp.gamma, inp.beta, inp.weight, inp.bias))
+        rm, rv = inp.running_mean.to(dev), inp.running_var.to(dev)
+        nbt = torch.zeros(1, dtype=torch.int64, device=dev)
+        out = None if host else torch.empty_like(x)
+        ws = torch.empty(api.prenorm_dilconv_residual_train_workspace_size(*x.shape, x.dtype),
+                         dtype=torch.uint8, device=dev)
+        tensors_in = (x, g, b, w, bias)
+
+        def call():
+            return api.prenorm_dilconv_residual_train(x, rm, rv, g, b, inp.eps, TRAIN_MOMENTUM,
+                                                      w, bias, inp.dilation,
+                                                      num_batches_tracked=nbt, out=out,
+                                                      workspace=ws)
+        out_shape = (x.shape, x.dtype)
     elif wl.kind == "conv_gn":
         x, w, g, b = map(place, (inp.x, inp.weight, inp.gamma, inp.beta))
         N, Cin, T = x.shape
@@ -425,6 +448,14 @@ def gpu_arm(args, world, rank, local):
     kernels = {k: dict(launches=len(v), mean_ms=round(statistics.mean(v), 5),
                        share=round(sum(v) / sum(sum(x) for x in per_kernel.values()), 4))
                for k, v in per_kernel.items()}
+    if "bn_row_stats" in per_kernel:
+        # the training-mode statistics pass: x read once, HBM-bound
+        st_ms = statistics.mean(per_kernel["bn_row_stats"])
+        cfg = info["config"]
+        x_bytes = cfg["N"] * cfg["C"] * cfg["L"] * (2 if info["dtype"] == "bf16" else 4)
+        roof["stats_kernel"] = dict(kernel="bn_row_stats", ms=round(st_ms, 5),
+                                    achieved_gbs=round(x_bytes / (st_ms * 1e-3) / 1e9, 1),
+                                    frac_of_hbm=round(x_bytes / (st_ms * 1e-3) / 1e9 / hbm_peak, 4))
     roof["kernel_timing"] = ("CUDA events around each launch, in a second timed pass of the "
                              f"same {steps} steps with the launch trace on "
                              f"({round(statistics.mean(trace_step_ms), 5)} ms/step traced)")
@@ -475,6 +506,18 @@ def oracle_sampler(name):
                                       inp.dilation, rn, ro)
             return 2.0 * C * 3 * L * k
         return run, "output rows (n, o, all L)", N * C
+    if wl.kind == "block_train":
+        N, C, L = inp.x.shape
+        x = inp.x.double().numpy()
+        w, b = inp.weight.double().numpy(), inp.bias.double().numpy()
+
+        def run(k):
+            # every sample repeats the whole statistics pass over x
+            oracle.prenorm_block_train(x, inp.running_mean, inp.running_var, inp.gamma,
+                                       inp.beta, inp.eps, TRAIN_MOMENTUM, w, b, inp.dilation,
+                                       rows_n=rng.integers(0, N, k), rows_o=rng.integers(0, C, k))
+            return 2.0 * C * 3 * L * k
+        return run, "output rows (n, o, all L) after the batch statistics", N * C
     if wl.kind == "conv_gn":
         N, Cin, T = inp.x.shape
         Cout, G = inp.weight.shape[0], inp.num_groups

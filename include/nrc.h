@@ -96,6 +96,43 @@ nrc_status nrc_prenorm_dilconv_residual(
     void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Pre-norm residual block with BatchNorm1d in TRAINING mode ("Kimi-K2.6
+ * l2_p12", the correctness discussion of batch against running statistics;
+ * the running-buffer update as "Kimi-K2.6 l2_p97" states it for BatchNorm1d)
+ *
+ *   mu[c]  = mean of x[:, c, :] over all N*L values
+ *   var[c] = mean of (x[:, c, :] - mu[c])^2 over the same values (biased)
+ *   out    = the block above with mu, var in place of running_mean, running_var
+ *   running_mean[c] <- (1 - bn_momentum)*running_mean[c] + bn_momentum*mu[c]
+ *   running_var[c]  <- (1 - bn_momentum)*running_var[c]
+ *                      + bn_momentum*var[c]*N*L/(N*L - 1)
+ *   *num_batches_tracked += 1
+ *
+ * Arguments as in nrc_prenorm_dilconv_residual, and:
+ * running_mean, running_var: (C) fp32 device buffers, read and updated in
+ *   place; either may be NULL (that buffer is neither read nor updated; the
+ *   output never depends on them).
+ * num_batches_tracked: one int64 on the device, or NULL.
+ * bn_momentum: finite (PyTorch's default is 0.1).  N*L >= 2.
+ * workspace: >= nrc_prenorm_dilconv_residual_train_workspace_size(N, C, L, dt)
+ *   bytes, 16-byte aligned: the eval block's workspace, then a (mean, M2)
+ *   partial per 2 KB segment of every row, and the batch mean and variance.
+ * Three steps on `stream`: a row-statistics kernel (x read once), a per-channel
+ * merge that writes the batch statistics and updates the buffers, then the
+ * eval-mode block's launches.  Every argument error returns before the first
+ * launch, so a rejected call leaves the buffers untouched.
+ * ------------------------------------------------------------------------ */
+size_t nrc_prenorm_dilconv_residual_train_workspace_size(int N, int C, int L, nrc_dtype dt);
+
+nrc_status nrc_prenorm_dilconv_residual_train(
+    const void *x, void *out, nrc_dtype dt, int N, int C, int L,
+    int kernel_size, int dilation, int padding,
+    float *bn_running_mean, float *bn_running_var, long long *num_batches_tracked,
+    const float *bn_gamma, const float *bn_beta, float bn_eps, float bn_momentum,
+    const void *conv_weight, const void *conv_bias,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Pre-norm residual block on HOST buffers.  Same computation and errors as
  * nrc_prenorm_dilconv_residual ("Kimi-K2.6 l2_p12", problem statement), for
  * callers whose x and out live in host memory.

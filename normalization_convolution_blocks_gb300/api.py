@@ -55,6 +55,9 @@ def load() -> ctypes.CDLL:
         "nrc_prenorm_dilconv_residual_workspace_size": ([i, i], sz),
         "nrc_prenorm_dilconv_residual": ([p, p, i, i, i, i, i, i, i, p, p, p, p, f, p, p, p, sz,
                                           p], i),
+        "nrc_prenorm_dilconv_residual_train_workspace_size": ([i, i, i, i], sz),
+        "nrc_prenorm_dilconv_residual_train": ([p, p, i, i, i, i, i, i, i, p, p, p, p, p, f, f, p,
+                                                p, p, sz, p], i),
         "nrc_prenorm_dilconv_residual_host_workspace_size": ([i, i, i, i, i], sz),
         "nrc_prenorm_dilconv_residual_host": ([p, p, i, i, i, i, i, i, i, p, p, p, p, f, p, p, i,
                                                p, sz, p], i),
@@ -166,6 +169,56 @@ def prenorm_dilconv_residual(x, bn_running_mean, bn_running_var, bn_gamma, bn_be
         _stream(stream))
     _check(st, "nrc_prenorm_dilconv_residual")
     _keep_alive(stream, xd, rm, rv, g, b, w, cb, ws)
+    return o
+
+
+def prenorm_dilconv_residual_train_workspace_size(N: int, C: int, L: int,
+                                                  dtype=torch.float32) -> int:
+    dt = NRC_F32 if dtype == torch.float32 else NRC_BF16
+    return int(load().nrc_prenorm_dilconv_residual_train_workspace_size(N, C, L, dt))
+
+
+def prenorm_dilconv_residual_train(x, bn_running_mean, bn_running_var, bn_gamma, bn_beta,
+                                   bn_eps, bn_momentum, conv_weight, conv_bias, dilation,
+                                   padding=None, kernel_size=3, num_batches_tracked=None,
+                                   out=None, workspace=None, stream=None):
+    """The block with BatchNorm1d in training mode: x is normalized with its
+    own per-channel mean and biased variance over (N, L), and the running
+    buffers (contiguous fp32 device tensors, or None) are updated in place
+    with the unbiased variance; num_batches_tracked (an int64 device tensor
+    or None) is incremented.  With x in host memory it is copied in, and the
+    result comes back as a host tensor (pinned)."""
+    lib = load()
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be float32 or bfloat16")
+    host = not x.is_cuda
+    dev = _target_device(x)
+    dt = NRC_F32 if x.dtype == torch.float32 else NRC_BF16
+    for t in (bn_running_mean, bn_running_var):
+        if t is not None and not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise TypeError("running statistics must be contiguous fp32 device tensors")
+    if num_batches_tracked is not None and not (num_batches_tracked.is_cuda and
+                                                num_batches_tracked.dtype == torch.int64):
+        raise TypeError("num_batches_tracked must be an int64 device tensor")
+    xd = _dev(x, dev)
+    N, C, L = xd.shape
+    g, b = (_dev(t, dev, torch.float32) for t in (bn_gamma, bn_beta))
+    w = _dev(conv_weight, dev, x.dtype)
+    cb = _dev(conv_bias, dev, x.dtype)
+    padding = dilation if padding is None else padding
+    o = out if (out is not None and not host) else torch.empty_like(xd)
+    ws = _workspace(lib.nrc_prenorm_dilconv_residual_train_workspace_size(N, C, L, dt), dev,
+                    workspace)
+    st = lib.nrc_prenorm_dilconv_residual_train(
+        _ptr(xd), _ptr(o), dt, N, C, L, kernel_size, dilation, padding, _ptr(bn_running_mean),
+        _ptr(bn_running_var), _ptr(num_batches_tracked), _ptr(g), _ptr(b), float(bn_eps),
+        float(bn_momentum), _ptr(w), _ptr(cb), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "nrc_prenorm_dilconv_residual_train")
+    _keep_alive(stream, xd, g, b, w, cb, ws)
+    if host:
+        res = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        res.copy_(o)
+        return res
     return o
 
 

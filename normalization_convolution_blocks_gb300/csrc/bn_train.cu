@@ -1,0 +1,321 @@
+// Pre-norm residual block with BatchNorm1d in training mode.
+//
+// Source: "Kimi-K2.6 l2_p12" (PopcornBench), the correctness discussion that
+// sets batch statistics against running statistics.  In training mode channel
+// c is normalized with the mean and the biased variance of x[:, c, :] over all
+// N*L values.  The running buffers move toward the batch values with the
+// unbiased variance ("Kimi-K2.6 l2_p97" states the same update for the
+// BatchNorm1d after its Linear).
+//
+// Three steps on the caller's stream:
+//   1. bn_row_stats_kernel: x is read once, in segments of 2 KB of a row; a
+//      warp computes each segment's (mean, M2) in two passes over registers.
+//   2. bn_train_finalize_kernel: one warp per channel merges its segments'
+//      partials (division-free pairwise-merge form, fp32), writes the batch
+//      mean and biased variance to the workspace and updates the running
+//      buffers and num_batches_tracked.  It is launched behind step 1
+//      (programmatic dependent launch) and waits for it at entry.
+//   3. The eval-mode block (nrc_prenorm_dilconv_residual) with the batch mean
+//      and variance in place of the running statistics.  Its first launch is an
+//      ordinary one, so it starts after step 2 has finished.
+//
+// Every argument error returns before the first launch, so a rejected call
+// leaves the running buffers untouched.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "nrc.h"
+#include "nrc_host.h"
+#include "nrc_launch.cuh"
+#include "nrc_ptx.cuh"
+
+namespace nrc {
+namespace {
+
+constexpr int kStatThreads = 256;
+
+// 16-byte loads of x: kVW elements each, decoded to fp32 from the raw words.
+template <typename T>
+struct StatVec;
+template <>
+struct StatVec<float> {
+    static constexpr int kVW = 4;
+    __device__ static float get(const uint4& r, int i) {
+        return __uint_as_float(i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w);
+    }
+    __device__ static float one(const float* p) { return __ldcs(p); }
+};
+template <>
+struct StatVec<__nv_bfloat16> {
+    static constexpr int kVW = 8;
+    __device__ static float get(const uint4& r, int i) {
+        const uint32_t w = (i >> 1) == 0 ? r.x : (i >> 1) == 1 ? r.y : (i >> 1) == 2 ? r.z : r.w;
+        return __uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16));
+    }
+    __device__ static float one(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Segments of 32*E elements (E per lane, E*sizeof(T) = 64 bytes) of each row
+// (n, c).  Warp w of the grid takes segments w, w + G, w + 2G, ... (G = warps
+// in the grid), so every SM streams the same share of x with no CTA-wide
+// barrier.  Per segment the warp computes its mean and M2 in two passes over
+// registers (two warp sums) and lane 0 writes (mean, M2) to
+// part[(c*N + n)*S + seg], S = segments per row; the last segment of a row
+// may be short.  VEC: rows start 16-byte aligned and L is a multiple of the
+// vector width, so whole 16-byte loads cover each segment (kept as raw words,
+// 16 registers a lane, and the next segment's 16 in flight); otherwise one
+// element per load.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kStatThreads)
+    bn_row_stats_kernel(const T* __restrict__ x, float2* __restrict__ part, int N, int C, int L,
+                        int S, int n_seg) {
+    griddep_launch_dependents();           // the finalize kernel may launch and wait
+    constexpr int VW = StatVec<T>::kVW;
+    constexpr int E = 4 * VW;              // four 16-byte loads per lane
+    constexpr int W = 32 * E;              // elements per segment
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (kStatThreads / 32);
+    const int first = blockIdx.x * (kStatThreads / 32) + (threadIdx.x >> 5);
+    auto seg_len = [&](int item) { return min(W, L - (item % S) * W); };
+    auto finish = [&](int item, float m, float q) {
+        q = warp_sum(q);
+        if (lane == 0) {
+            const int row = item / S, seg = item - row * S;
+            const int n = row / C, c = row - n * C;
+            part[((size_t)c * N + n) * S + seg] = make_float2(m, q);
+        }
+    };
+    if constexpr (VEC) {
+        // The next segment's loads are issued before this one's sums, so each
+        // warp keeps a segment in flight while it reduces.
+        auto load = [&](int item, uint4 (&r)[4]) {
+            const int here = seg_len(item);
+            const T* xs = x + (size_t)(item / S) * L + (size_t)(item % S) * W;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = (j * 32 + lane) * VW;
+                r[j] = e < here ? __ldcs(reinterpret_cast<const uint4*>(xs + e))
+                                : make_uint4(0u, 0u, 0u, 0u);      // reads as 0.0
+            }
+        };
+        uint4 r[4];
+        if (first < n_seg) load(first, r);
+        for (int item = first; item < n_seg; item += warps) {
+            uint4 rn[4];
+            if (item + warps < n_seg) {
+                load(item + warps, rn);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) rn[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            const int here = seg_len(item);
+            float s = 0.f, q = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < VW; ++i) s += StatVec<T>::get(r[j], i);
+            const float m = warp_sum(s) / (float)here;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool ok = (j * 32 + lane) * VW < here;
+#pragma unroll
+                for (int i = 0; i < VW; ++i) {
+                    const float d = ok ? StatVec<T>::get(r[j], i) - m : 0.f;
+                    q = fmaf(d, d, q);
+                }
+            }
+            finish(item, m, q);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) r[j] = rn[j];
+        }
+    } else {
+        for (int item = first; item < n_seg; item += warps) {
+            const int here = seg_len(item);
+            const T* xs = x + (size_t)(item / S) * L + (size_t)(item % S) * W;
+            float v[E];
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+                const int e = j * 32 + lane;
+                v[j] = e < here ? StatVec<T>::one(xs + e) : 0.f;
+            }
+            float s = 0.f, q = 0.f;
+#pragma unroll
+            for (int j = 0; j < E; ++j) s += v[j];
+            const float m = warp_sum(s) / (float)here;
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+                const float d = j * 32 + lane < here ? v[j] - m : 0.f;
+                q = fmaf(d, d, q);
+            }
+            finish(item, m, q);
+        }
+    }
+}
+
+// Resident CTAs per SM of a statistics kernel (queried once): the grid is one
+// full wave, so no CTA starts late and streams alone at the end.
+template <typename T, bool VEC>
+int stats_ctas_per_sm() {
+    static const int n = [] {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, bn_row_stats_kernel<T, VEC>,
+                                                          kStatThreads, 0) != cudaSuccess ||
+            b < 1)
+            b = 1;
+        return b;
+    }();
+    return n;
+}
+
+// One warp per channel merges its N*S segment partials: with k_i values in
+// segment i (W, or the row's remainder for the last one),
+//   mean = sum_i k_i mean_i / (N L),   M2 = sum_i (M2_i + k_i (mean_i - mean)^2).
+__global__ void __launch_bounds__(256)
+    bn_train_finalize_kernel(const float2* __restrict__ part, int N, int C, int L, int S, int W,
+                             float* __restrict__ batch_mean, float* __restrict__ batch_var,
+                             float* running_mean, float* running_var,
+                             long long* num_batches_tracked, float momentum) {
+    griddep_wait();                        // the segment statistics are complete
+    const int c = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (c == 0 && lane == 0 && num_batches_tracked) *num_batches_tracked += 1;
+    if (c >= C) return;
+    const float2* pc = part + (size_t)c * N * S;
+    const int total = N * S;
+    const float last = (float)(L - (S - 1) * W);   // values in a row's last segment
+    float s = 0.f;
+    for (int i = lane; i < total; i += 32) {
+        const float k = (i % S == S - 1) ? last : (float)W;
+        s = fmaf(k, pc[i].x, s);
+    }
+    const float cnt = (float)N * (float)L;
+    const float mean = warp_sum(s) / cnt;
+    float q = 0.f;
+    for (int i = lane; i < total; i += 32) {
+        const float k = (i % S == S - 1) ? last : (float)W;
+        const float2 p = pc[i];
+        const float d = p.x - mean;
+        q += p.y + k * d * d;
+    }
+    q = warp_sum(q);
+    if (lane != 0) return;
+    const float var = q / cnt;             // biased: normalizes the batch
+    batch_mean[c] = mean;
+    batch_var[c] = var;
+    if (running_mean) running_mean[c] = (1.f - momentum) * running_mean[c] + momentum * mean;
+    if (running_var)
+        running_var[c] = (1.f - momentum) * running_var[c] + momentum * (q / (cnt - 1.f));
+}
+
+// Segment length of the statistics kernel, in elements.
+inline int stat_segment(nrc_dtype dt) { return 32 * 4 * (dt == NRC_F32 ? 4 : 8); }
+
+inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct TrainLayout {
+    size_t part, mean, var, total;
+};
+
+TrainLayout train_layout(int N, int C, int L, nrc_dtype dt) {
+    TrainLayout t{};
+    const size_t base = nrc_prenorm_dilconv_residual_workspace_size(C, dt);
+    if (base == 0 || N <= 0 || L <= 0) return t;
+    const size_t S = (size_t)ceil_div(L, stat_segment(dt));
+    t.part = align256(base);
+    t.mean = align256(t.part + (size_t)N * C * S * sizeof(float2));
+    t.var = align256(t.mean + (size_t)C * sizeof(float));
+    t.total = t.var + (size_t)C * sizeof(float);
+    return t;
+}
+
+}  // namespace
+}  // namespace nrc
+
+using namespace nrc;
+
+extern "C" size_t nrc_prenorm_dilconv_residual_train_workspace_size(int N, int C, int L,
+                                                                   nrc_dtype dt) {
+    return train_layout(N, C, L, dt).total;
+}
+
+extern "C" nrc_status nrc_prenorm_dilconv_residual_train(
+    const void* x, void* out, nrc_dtype dt, int N, int C, int L, int kernel_size, int dilation,
+    int padding, float* running_mean, float* running_var, long long* num_batches_tracked,
+    const float* gamma, const float* beta, float bn_eps, float bn_momentum,
+    const void* conv_weight, const void* conv_bias, void* workspace, size_t workspace_bytes,
+    void* stream) {
+    // The eval-mode entry's checks, made here before anything is launched.
+    if (dt != NRC_F32 && dt != NRC_BF16) return NRC_ERR_INVALID_ARG;
+    if (!x || !out || !gamma || !beta || !conv_weight || !workspace) return NRC_ERR_INVALID_ARG;
+    if (N <= 0 || C <= 0 || L <= 0 || dilation <= 0 || padding < 0) return NRC_ERR_INVALID_ARG;
+    if (!(bn_eps >= 0.f) || !std::isfinite(bn_eps)) return NRC_ERR_INVALID_ARG;
+    if (!std::isfinite(bn_momentum)) return NRC_ERR_INVALID_ARG;
+    if ((long long)N * L < 2) return NRC_ERR_INVALID_ARG;     // unbiased variance: N*L - 1
+    if (kernel_size != 3 || padding != dilation) return NRC_ERR_UNSUPPORTED;
+    if (C > 2048) return NRC_ERR_UNSUPPORTED;
+    const size_t esz = dt == NRC_F32 ? 4 : 2;
+    const size_t bytes = (size_t)N * C * L * esz;
+    if (ranges_overlap(x, bytes, out, bytes)) return NRC_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return NRC_ERR_ALIGNMENT;
+    const TrainLayout lay = train_layout(N, C, L, dt);
+    if (workspace_bytes < lay.total) return NRC_ERR_WORKSPACE;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float2* part = reinterpret_cast<float2*>(ws + lay.part);
+    float* bmean = reinterpret_cast<float*>(ws + lay.mean);
+    float* bvar = reinterpret_cast<float*>(ws + lay.var);
+    const int vw = dt == NRC_F32 ? 4 : 8;
+    const int vec = (L % vw == 0 && aligned(x, 16)) ? 1 : 0;
+    const int W = stat_segment(dt);
+    const int S = ceil_div(L, W);
+    const long long n_seg = (long long)N * C * S;
+    // 32-bit segment indices with room for one grid stride (x would be ~4 TB)
+    if (n_seg >= (1LL << 31) - (1LL << 24)) return NRC_ERR_UNSUPPORTED;
+    {
+        TraceScope ts("bn_row_stats", st);
+        // one wave of resident CTAs striding over the segments
+        const int per_sm = dt == NRC_F32 ? (vec ? stats_ctas_per_sm<float, true>()
+                                                : stats_ctas_per_sm<float, false>())
+                                         : (vec ? stats_ctas_per_sm<__nv_bfloat16, true>()
+                                                : stats_ctas_per_sm<__nv_bfloat16, false>());
+        const long long want = (n_seg + kStatThreads / 32 - 1) / (kStatThreads / 32);
+        const unsigned grid = (unsigned)std::max<long long>(
+            1, std::min<long long>(want, (long long)device_sm_count() * per_sm));
+        const float* xf = static_cast<const float*>(x);
+        const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+        if (dt == NRC_F32 && vec)
+            bn_row_stats_kernel<float, true><<<grid, kStatThreads, 0, st>>>(xf, part, N, C, L, S,
+                                                                             (int)n_seg);
+        else if (dt == NRC_F32)
+            bn_row_stats_kernel<float, false><<<grid, kStatThreads, 0, st>>>(xf, part, N, C, L,
+                                                                              S, (int)n_seg);
+        else if (vec)
+            bn_row_stats_kernel<__nv_bfloat16, true><<<grid, kStatThreads, 0, st>>>(
+                xb, part, N, C, L, S, (int)n_seg);
+        else
+            bn_row_stats_kernel<__nv_bfloat16, false><<<grid, kStatThreads, 0, st>>>(
+                xb, part, N, C, L, S, (int)n_seg);
+        if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
+    }
+    {
+        TraceScope ts("bn_train_finalize", st);
+        if (launch_after_prev(bn_train_finalize_kernel, dim3((unsigned)ceil_div(C, 8)), dim3(256),
+                              st, (const float2*)part, N, C, L, S, W, bmean, bvar,
+                              running_mean, running_var, num_batches_tracked,
+                              bn_momentum) != cudaSuccess)
+            return NRC_ERR_CUDA;
+    }
+    return nrc_prenorm_dilconv_residual(x, out, dt, N, C, L, kernel_size, dilation, padding,
+                                        bmean, bvar, gamma, beta, bn_eps, conv_weight, conv_bias,
+                                        ws, lay.part, stream);
+}

@@ -12,7 +12,9 @@ identity:
 
 * pre-norm block: x ~N(0,1); running_mean ~U(-0.5,0.5); running_var
   ~U(0.5,2); gamma ~U(0.5,1.5); beta ~U(-0.5,0.5); conv weight and bias
-  ~U(+-1/sqrt(3C)).  Draw order: x, rm, rv, gamma, beta, W, bias.
+  ~U(+-1/sqrt(3C)).  Draw order: x, rm, rv, gamma, beta, W, bias.  The
+  training-mode workload draws the same tensors (rm, rv are then the running
+  buffers' starting values; BatchNorm momentum 0.1).
 * conv + GroupNorm: x ~N(0,1); W ~U(+-1/sqrt(3*C_in)); gamma ~U(0.5,1.5);
   beta ~U(-0.5,0.5).  Draw order: x, W, gamma, beta.
 * Linear + BN + bias + divide + Swish: x ~N(0,1); W, b_lin ~U(+-1/sqrt(IN));
@@ -129,12 +131,12 @@ def linear_bn_swish_inputs(B, IN, OUT, seed=0, random_affine=False, eps=1e-5,
 class Workload:
     """A named workload: which block, and its sizes."""
     name: str
-    kind: str                      # "block" | "conv_gn" | "linear"
+    kind: str                      # "block" | "block_train" | "conv_gn" | "linear"
     params: dict = field(default_factory=dict)
 
     def make(self, seed=0):
         p = dict(self.params)
-        if self.kind == "block":
+        if self.kind in ("block", "block_train"):
             dt = torch.bfloat16 if p.pop("dtype", "f32") == "bf16" else torch.float32
             return prenorm_block_inputs(p["N"], p["C"], p["L"], p["dilation"], seed=seed,
                                         dtype=dt)
@@ -152,6 +154,8 @@ WORKLOADS = {
                                        dict(N=2, C=32, L=512, dilation=128)),
     "prenorm_block_f32": Workload("prenorm_block_f32", "block",
                                   dict(N=32, C=256, L=4096, dilation=128)),
+    "prenorm_block_train_f32": Workload("prenorm_block_train_f32", "block_train",
+                                        dict(N=32, C=256, L=4096, dilation=128)),
     "conv1d_groupnorm_f32": Workload("conv1d_groupnorm_f32", "conv_gn",
                                      dict(N=16, Cin=128, Cout=256, T=1024, G=32)),
     "linear_bn_swish_f32": Workload("linear_bn_swish_f32", "linear",

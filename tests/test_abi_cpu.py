@@ -86,6 +86,53 @@ def test_block_validation(lib, kw, expect):
     assert _block(lib, **kw) == expect
 
 
+def _train(lib, **kw):
+    a = dict(x=FAKE, out=FAKE2, dt=0, N=2, C=32, L=64, k=3, d=4, pad=4, rm=FAKE, rv=FAKE,
+             nbt=None, g=FAKE, b=FAKE, eps=1e-5, m=0.1, w=FAKE, bias=FAKE, ws=WS, wsb=1 << 30,
+             stream=None)
+    a.update(kw)
+    return lib.nrc_prenorm_dilconv_residual_train(
+        a["x"], a["out"], a["dt"], a["N"], a["C"], a["L"], a["k"], a["d"], a["pad"], a["rm"],
+        a["rv"], a["nbt"], a["g"], a["b"], a["eps"], a["m"], a["w"], a["bias"], a["ws"],
+        a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), 1), (dict(out=None), 1), (dict(g=None), 1), (dict(w=None), 1),
+    (dict(ws=None), 1), (dict(N=0), 1), (dict(L=-1), 1), (dict(d=0, pad=0), 1),
+    (dict(dt=7), 1), (dict(eps=-1.0), 1), (dict(m=float("nan")), 1), (dict(m=float("inf")), 1),
+    (dict(N=1, L=1, d=1, pad=1), 1),                           # one value per channel
+    (dict(k=5), 2), (dict(pad=3), 2), (dict(C=4096), 2),
+    (dict(out=ctypes.c_void_p(0x10000000 + 64)), 1),          # out overlaps x
+    (dict(ws=ctypes.c_void_p(0x30000004)), 3),                 # misaligned workspace
+    (dict(wsb="eval"), 4),                                     # the eval block's share only
+    (dict(wsb="one short"), 4),
+])
+def test_train_block_validation(lib, kw, expect):
+    """The training-mode entry rejects bad arguments before its first launch
+    (the running buffers are never touched by a rejected call)."""
+    if kw.get("wsb") == "eval":
+        kw = dict(wsb=lib.nrc_prenorm_dilconv_residual_workspace_size(32, 0))
+    elif kw.get("wsb") == "one short":
+        kw = dict(wsb=lib.nrc_prenorm_dilconv_residual_train_workspace_size(2, 32, 64, 0) - 1)
+    assert _train(lib, **kw) == expect
+
+
+def test_train_workspace_query(lib):
+    from normalization_convolution_blocks_gb300 import api
+    f = lib.nrc_prenorm_dilconv_residual_train_workspace_size
+    base = api.prenorm_dilconv_residual_workspace_size(256)
+    # eval workspace, then 256-aligned: a (mean, M2) pair per 2 KB segment of each
+    # of the N*C rows (L=4096 fp32: 8 segments), C means, C variances
+    part = (base + 255) // 256 * 256
+    mean = (part + 32 * 256 * 8 * 8 + 255) // 256 * 256
+    var = (mean + 256 * 4 + 255) // 256 * 256
+    assert f(32, 256, 4096, 0) == var + 256 * 4
+    assert f(32, 256, 4097, 0) > f(32, 256, 4096, 0)            # a ninth, short segment
+    assert f(0, 256, 64, 0) == 0 and f(32, 0, 64, 0) == 0 and f(32, 256, 0, 0) == 0
+    assert f(32, 256, 64, 9) == 0
+
+
 def _gn(lib, **kw):
     a = dict(x=FAKE, out=FAKE2, N=2, Cin=8, Cout=16, T=32, k=3, s=1, p=1, d=1, w=FAKE, bias=None,
              G=4, g=FAKE, b=FAKE, eps=1e-5, ws=WS, wsb=1 << 30, stream=None)
