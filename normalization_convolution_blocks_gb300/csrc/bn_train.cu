@@ -72,10 +72,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 // part[(c*N + n)*S + seg], S = segments per row; the last segment of a row
 // may be short.  VEC: rows start 16-byte aligned and L is a multiple of the
 // vector width, so whole 16-byte loads cover each segment (kept as raw words,
-// 16 registers a lane, and the next segment's 16 in flight); otherwise one
-// element per load.
+// 16 registers a lane); otherwise one element per load.  No CTA-wide barrier,
+// and the fp32 vector path fits 32 registers, so 64 warps per SM keep their
+// loads in flight (bf16 decodes more per load and stays at 64 registers).
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kStatThreads)
+__global__ void __launch_bounds__(kStatThreads, (VEC && sizeof(T) == 4) ? 8 : 1)
     bn_row_stats_kernel(const T* __restrict__ x, float2* __restrict__ part, int N, int C, int L,
                         int S, int n_seg) {
     griddep_launch_dependents();           // the finalize kernel may launch and wait
@@ -95,29 +96,16 @@ __global__ void __launch_bounds__(kStatThreads)
         }
     };
     if constexpr (VEC) {
-        // The next segment's loads are issued before this one's sums, so each
-        // warp keeps a segment in flight while it reduces.
-        auto load = [&](int item, uint4 (&r)[4]) {
+        for (int item = first; item < n_seg; item += warps) {
             const int here = seg_len(item);
             const T* xs = x + (size_t)(item / S) * L + (size_t)(item % S) * W;
+            uint4 r[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int e = (j * 32 + lane) * VW;
                 r[j] = e < here ? __ldcs(reinterpret_cast<const uint4*>(xs + e))
                                 : make_uint4(0u, 0u, 0u, 0u);      // reads as 0.0
             }
-        };
-        uint4 r[4];
-        if (first < n_seg) load(first, r);
-        for (int item = first; item < n_seg; item += warps) {
-            uint4 rn[4];
-            if (item + warps < n_seg) {
-                load(item + warps, rn);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) rn[j] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            const int here = seg_len(item);
             float s = 0.f, q = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -134,8 +122,6 @@ __global__ void __launch_bounds__(kStatThreads)
                 }
             }
             finish(item, m, q);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) r[j] = rn[j];
         }
     } else {
         for (int item = first; item < n_seg; item += warps) {
