@@ -74,7 +74,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // vector width, so whole 16-byte loads cover each segment (kept as raw words,
 // 16 registers a lane); otherwise one element per load.  No CTA-wide barrier,
 // and the fp32 vector path fits 32 registers, so 64 warps per SM keep their
-// loads in flight (bf16 decodes more per load and stays at 64 registers).
+// loads in flight (bf16 decodes two values per word and needs more).
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kStatThreads, (VEC && sizeof(T) == 4) ? 8 : 1)
     bn_row_stats_kernel(const T* __restrict__ x, float2* __restrict__ part, int N, int C, int L,
