@@ -233,8 +233,9 @@ nrc_status nrc_conv1d_groupnorm(
  *   u   = ((y - mu)/sqrt(var + eps) * gamma + beta + *add_bias) / divide_value
  *   out = u * sigmoid(u)
  *
- * x: (B, in_f) fp32.  out: (B, out_f) fp32 (holds y between kernels), no
- * overlap with x.  lin_weight: (out_f, in_f).  lin_bias: (out_f) or NULL.
+ * x: (B, in_f) fp32.  out: (B, out_f) fp32, no overlap with x; in training
+ * mode it holds y between kernels, in eval mode the GEMM's epilogue writes the
+ * result straight into it (one GEMM launch after the x repack, y never stored).  lin_weight: (out_f, in_f).  lin_bias: (out_f) or NULL.
  * bn_gamma/bn_beta: (out_f) or both NULL (1 and 0).  running_mean/var:
  * (out_f), read in eval mode, read and updated in place in training mode.
  * num_batches_tracked: one int64 or NULL.  add_bias: DEVICE pointer to one

@@ -12,11 +12,13 @@
 // and keeps the column's (count, mean, M2) over the tile's batch rows, so the
 // batch statistics need no cross-thread reduction.
 //
-// Launches per call: pack x -> GEMM (y + per-tile column statistics) ->
-// finalize (batch mean/var, running-stat update) -> normalize + bias +
-// divide + Swish in place.  Each of the last three is launched behind the one
-// before it (programmatic dependent launch) and waits for it before reading
-// its results.
+// Launches per call in training mode: pack x -> GEMM (y + per-tile column
+// statistics) -> finalize (batch mean/var, running-stat update) -> normalize
+// + bias + divide + Swish in place.  Each of the last three is launched behind
+// the one before it (programmatic dependent launch) and waits for it before
+// reading its results.  In eval mode the statistics are the running buffers,
+// known before the GEMM starts, so the whole chain is the GEMM's epilogue:
+// pack x -> GEMM writing out directly (y never reaches memory).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -33,6 +35,14 @@ struct LinearParams {
     float* out;              // (B, OUT): receives y
     const float* lin_bias;   // (OUT) or NULL
     float4* partials;        // [bt * OUT + j] = (count, mean, M2, 0)
+    // eval mode (the epilogue applies BN with the running statistics, the
+    // scalar bias, the divide and Swish)
+    const float* running_mean;
+    const float* running_var;
+    const float* gamma;      // NULL with beta NULL: affine off
+    const float* beta;
+    const float* add_bias;   // one element on the device
+    float bn_eps, divide_value;
     int B, IN, OUT;
     int n_jt, n_bt, n_kiters, BN;
     int vec_ok;              // W 16-byte aligned and IN % 4 == 0
@@ -42,7 +52,9 @@ struct LinearTile {
     int jt, bt;
 };
 
-template <bool STAGED>
+__device__ __forceinline__ float swish_f(float u) { return u / (1.0f + expf(-u)); }
+
+template <bool STAGED, bool EVAL = false>
 struct LinearProblem {
     using Params = LinearParams;
     using Tile = LinearTile;
@@ -121,13 +133,43 @@ struct LinearProblem {
                                                     const Tile& tl, int quarter, int lane,
                                                     uint32_t taddr, int BN, int halves,
                                                     Acquire& acquire, Release& release) {
-        for (int h = 0; h < halves; ++h)
-            if (!acquire(h)) return false;
         const int j = tl.jt * kBM + quarter * 32 + lane;
         const bool j_ok = j < p.OUT;
-        const float lb = (j_ok && p.lin_bias) ? __ldg(p.lin_bias + j) : 0.f;
         const int b0 = tl.bt * BN;
         const int bvalid = p.B - b0;               // batch rows of this tile that exist
+        if constexpr (EVAL) {
+            // u = (y - mu_j) * scale_j + shift_j with the running statistics
+            // (the same coefficients the finalize kernel forms), out = swish(u)
+            float lb = 0.f, c = 0.f, sc = 0.f, sh = 0.f;
+            if (j_ok) {
+                lb = p.lin_bias ? __ldg(p.lin_bias + j) : 0.f;
+                c = __ldg(p.running_mean + j);
+                const float inv = 1.0f / sqrtf(__ldg(p.running_var + j) + p.bn_eps);
+                const float g = p.gamma ? __ldg(p.gamma + j) : 1.f;
+                const float be = p.beta ? __ldg(p.beta + j) : 0.f;
+                sc = g * inv / p.divide_value;
+                sh = (be + __ldg(p.add_bias)) / p.divide_value;
+            }
+            for (int h = 0; h < halves; ++h)
+                if (!acquire(h)) return false;
+            float* outj = p.out + (size_t)b0 * p.OUT + j;
+            for (int cc = 0; cc < BN && cc < bvalid; cc += 16) {
+                float v[16];
+                tmem_ld16(taddr + (uint32_t)cc, v);
+                const int n = min(16, bvalid - cc);   // uniform
+                float* op = outj + (size_t)cc * p.OUT;
+                if (j_ok) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (i < n) op[(size_t)i * p.OUT] = swish_f(fmaf(v[i] + lb - c, sc, sh));
+                }
+            }
+            for (int h = 0; h < halves; ++h) release(h);
+            return true;
+        }
+        for (int h = 0; h < halves; ++h)
+            if (!acquire(h)) return false;
+        const float lb = (j_ok && p.lin_bias) ? __ldg(p.lin_bias + j) : 0.f;
         float cnt = 0.f, mean = 0.f, m2 = 0.f;
         float* outj = p.out + (size_t)b0 * p.OUT + j;
         for (int cc = 0; cc < BN && cc < bvalid; cc += 16) {
@@ -244,8 +286,6 @@ __global__ void bn_finalize_kernel(const float4* __restrict__ partials, int n_bt
     colp[OUT + j] = g * inv / divide_value;
     colp[2 * OUT + j] = (be + add_bias[0]) / divide_value;
 }
-
-__device__ __forceinline__ float swish_f(float u) { return u / (1.0f + expf(-u)); }
 
 // out[b][j] = swish((y - mean_j) * scale_j + shift_j), in place.  Threads of
 // grid x own 4-column groups (their coefficients stay in registers), grid y
@@ -377,6 +417,19 @@ extern "C" nrc_status nrc_linear_bn_swish(
     }
     if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
     pl.g.b_after_prev = true;          // launched behind the x repack
+    if (!training) {
+        // eval: one GEMM whose epilogue writes out; the running statistics are
+        // inputs here, so nothing else runs
+        p.running_mean = bn_running_mean;
+        p.running_var = bn_running_var;
+        p.gamma = bn_gamma;
+        p.beta = bn_beta;
+        p.add_bias = add_bias;
+        p.bn_eps = bn_eps;
+        p.divide_value = divide_value;
+        return staged ? launch_gemm<LinearProblem<true, true>, 2>("linear_gemm", p, pl.g, st)
+                      : launch_gemm<LinearProblem<false, true>, 2>("linear_gemm", p, pl.g, st);
+    }
     nrc_status s = staged ? launch_gemm<LinearProblem<true>, 2>("linear_gemm", p, pl.g, st)
                           : launch_gemm<LinearProblem<false>, 2>("linear_gemm", p, pl.g, st);
     if (s != NRC_OK) return s;

@@ -79,6 +79,43 @@ def test_eval_mode_and_divide():
     _check(_gpu(dev, li, training=False), _ref(li, training=False), "eval, divide 2.5")
 
 
+@pytest.mark.parametrize("B,IN,OUT,affine", [
+    (1, 64, 32, True),        # one batch row: allowed in eval mode
+    (100, 100, 70, True),     # ragged everywhere
+    (33, 37, 50, True),       # W rows loaded directly, not by TMA
+    (300, 520, 200, True),    # two batch tiles, ragged
+    (64, 256, 128, False),    # affine off
+])
+def test_eval_shapes(B, IN, OUT, affine):
+    """Eval mode runs as one GEMM whose epilogue applies BN with the running
+    statistics, the scalar bias, the divide and Swish."""
+    dev = need_gpu()
+    li = syn.linear_bn_swish_inputs(B, IN, OUT, seed=B * 3 + IN + OUT, random_affine=affine)
+    g = torch.Generator().manual_seed(B + OUT)
+    li.running_mean = torch.randn(OUT, generator=g) * 0.1
+    li.running_var = torch.rand(OUT, generator=g) + 0.5
+    li.divide_value = 1.5
+    _check(_gpu(dev, li, training=False), _ref(li, training=False), f"eval B{B} IN{IN} OUT{OUT}")
+
+
+def test_eval_multi_wave_and_full_workload_sampled_columns():
+    dev = need_gpu()
+    for li, tag in ((syn.linear_bn_swish_inputs(256, 128, 20480, seed=9, random_affine=True),
+                     "eval multi-wave"),
+                    (syn.WORKLOADS["linear_bn_swish_f32"].make(seed=0), "eval full workload")):
+        OUT = li.weight.shape[0]
+        g = torch.Generator().manual_seed(OUT)
+        li.running_mean = torch.randn(OUT, generator=g) * 0.05
+        li.running_var = torch.rand(OUT, generator=g) * 0.1 + 0.05
+        out, rm, rv = _gpu(dev, li, training=False)
+        cols = np.unique(np.concatenate([[0, 127, 128, OUT - 1],
+                                         np.random.default_rng(OUT).integers(0, OUT, 60)]))
+        r_out, _, _, _ = _ref(li, training=False, cols=cols)
+        assert_f32(out[:, cols], r_out, tag)
+        assert np.array_equal(rm, li.running_mean.double().numpy())    # untouched
+        assert np.array_equal(rv, li.running_var.double().numpy())
+
+
 def test_num_batches_tracked_increments():
     dev = need_gpu()
     li = syn.linear_bn_swish_inputs(16, 32, 16, seed=6)
