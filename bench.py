@@ -120,8 +120,8 @@ def workload_info(name):
         B, IN, OUT = p["B"], p["IN"], p["OUT"]
         flops = 2.0 * B * IN * OUT
         min_bytes = 4 * (B * IN + OUT * IN + B * OUT + 5 * OUT)
-        cfg = dict(workload=name, B=B, in_features=IN, out_features=OUT, bn="training",
-                   storage="f32")
+        cfg = dict(workload=name, B=B, in_features=IN, out_features=OUT,
+                   bn="training" if p.get("training", True) else "eval", storage="f32")
         dtype = "f32"
         main = "linear_gemm"
     return dict(flops=flops, min_bytes=min_bytes, config=cfg, dtype=dtype, main_kernel=main,
@@ -334,9 +334,11 @@ def make_call(name, dev, host=False):
                                            dtype=torch.uint8, device=dev)
         tensors_in = (x, w, lb, g, b, ab)
 
+        training = wl.params.get("training", True)
+
         def call():
             return api.linear_bn_swish(x, w, lb, g, b, rm, rv, ab, inp.divide_value, inp.eps,
-                                       inp.momentum, True, nbt, out=out, workspace=ws)
+                                       inp.momentum, training, nbt, out=out, workspace=ws)
         out_shape = ((B, OUT), torch.float32)
     h2d = sum(t.numel() * t.element_size() for t in tensors_in if t is not None)
     d2h = math.prod(out_shape[0]) * (2 if out_shape[1] == torch.bfloat16 else 4)
@@ -531,10 +533,11 @@ def oracle_sampler(name):
     B, IN = inp.x.shape
     OUT = inp.weight.shape[0]
     x, w = inp.x.double().numpy(), inp.weight.double().numpy()
+    training = wl.params.get("training", True)
 
     def run(k):
         oracle.linear_bn_swish(x, w, inp.lin_bias, inp.gamma, inp.beta, inp.running_mean,
-                               inp.running_var, inp.eps, inp.momentum, True,
+                               inp.running_var, inp.eps, inp.momentum, training,
                                float(inp.add_bias[0]), inp.divide_value,
                                cols=rng.integers(0, OUT, k))
         return 2.0 * B * IN * k

@@ -21,6 +21,8 @@ identity:
   gamma = 1, beta = 0 (module defaults) unless ``random_affine``, then
   gamma ~U(0.5,1.5), beta ~U(-0.5,0.5); running stats 0 and 1; the added
   scalar bias ~N(0,1).  Draw order: x, W, b_lin, [gamma, beta], add_bias.
+  The eval-mode workload draws the same tensors and normalizes with the
+  running statistics (0 and 1).
 
 bf16 storage: the fp32 draw is rounded to bf16 once (round to nearest even by
 ``Tensor.to``); both sides then read the same bf16 values.
@@ -160,6 +162,8 @@ WORKLOADS = {
                                      dict(N=16, Cin=128, Cout=256, T=1024, G=32)),
     "linear_bn_swish_f32": Workload("linear_bn_swish_f32", "linear",
                                     dict(B=1024, IN=8192, OUT=8192)),
+    "linear_bn_swish_eval_f32": Workload("linear_bn_swish_eval_f32", "linear",
+                                         dict(B=1024, IN=8192, OUT=8192, training=False)),
 }
 for _C in (256, 512):
     for _d in (1, 8, 128, 512):
