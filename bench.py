@@ -541,7 +541,8 @@ def oracle_sampler(name):
                                float(inp.add_bias[0]), inp.divide_value,
                                cols=rng.integers(0, OUT, k))
         return 2.0 * B * IN * k
-    return run, "output columns (all batch rows, BN over the batch)", OUT
+    return run, ("output columns (all batch rows, BN over the batch)" if training else
+                 "output columns (all batch rows, BN with the running statistics)"), OUT
 
 
 def size_sample(run, seconds):
