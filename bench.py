@@ -52,7 +52,7 @@ L2_FLUSH_BYTES = 256 << 20
 NCU_TRAFFIC = {
     "prenorm_block_f32": {"bytes": 221508096, "src_hash": "41640fe1382ffc87",
                           "profile": "profiles/gemm_prenorm_block_f32_N32_C256_L4096_d128.md"},
-    "linear_bn_swish_f32": {"bytes": 358642688, "src_hash": "779716fe7b7bbb47",
+    "linear_bn_swish_f32": {"bytes": 358875904, "src_hash": "eaf8aff3fa6e305a",
                             "profile": "profiles/gemm_linear_bn_swish_f32_B1024_IN8192_OUT8192.md"},
     "prenorm_block_train_f32": {"bytes": 221418240, "src_hash": "41640fe1382ffc87",
                                 "profile": "profiles/prenorm_block_train_f32_N32_C256_L4096_d128.md"},
