@@ -124,8 +124,26 @@ def workload_info(name):
                    bn="training" if p.get("training", True) else "eval", storage="f32")
         dtype = "f32"
         main = "linear_gemm"
+    if wl.kind in ("block", "block_train"):
+        largest = ("x", esz * N * C * L)
+    elif wl.kind == "conv_gn":
+        largest = ("out", 4 * N * Cout * T)
+    else:
+        largest = ("W", 4 * OUT * IN)
     return dict(flops=flops, min_bytes=min_bytes, config=cfg, dtype=dtype, main_kernel=main,
-                kind=wl.kind)
+                kind=wl.kind, largest_tensor=largest)
+
+
+L2_BYTES = 129 * 1000 * 1000      # GB300 L2 (126 MiB)
+
+
+def l2_note(info):
+    name, nbytes = info["largest_tensor"]
+    note = f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write, untimed)"
+    if nbytes > L2_BYTES:
+        return note + f"; {name} alone ({nbytes / 1e6:.0f} MB) exceeds L2 on this workload"
+    return note + f"; the largest tensor ({name}, {nbytes / 1e6:.1f} MB) fits in L2, so the flush " \
+                  "is what keeps the steps cold"
 
 
 def roofline_peaks(info, peaks):
@@ -629,8 +647,7 @@ def main():
         steps=r["steps"], warmup=args.warmup, ms_per_step=round(r["ms_per_step"], 5),
         higher_is_better=True, scaling="weak", vs_baseline=None, dtype=info["dtype"],
         data="synthetic",
-        config=dict(info["config"], l2=f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB "
-                                        "write, untimed); x alone exceeds L2 on this workload",
+        config=dict(info["config"], l2=l2_note(info),
                     parallelism="replicas" if world > 1 else "single GPU",
                     arithmetic=("bf16 tensor products, fp32 accumulate" if info["dtype"] == "bf16"
                                 else "3 bf16 tensor products per term (hi/lo split), "
@@ -639,6 +656,10 @@ def main():
         clocks=r["clocks"],
         ms_per_call_p10=round(r["step_ms_p10"], 5), ms_per_call_p90=round(r["step_ms_p90"], 5),
         kernels=r["kernels"],
+        bandwidth=dict(value=round(world * info["min_bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1),
+                       unit="GB/s", bytes_per_call=info["min_bytes"],
+                       note="the call's algorithmic bytes (inputs read once, output written "
+                            "once) over its untraced time"),
     )
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)

@@ -56,3 +56,37 @@ def test_recorded_dram_counters_name_committed_profiles():
         assert name in syn.WORKLOADS
         assert os.path.exists(os.path.join(ROOT, rec["profile"])), rec["profile"]
         assert rec["bytes"] > 0 and len(rec["src_hash"]) == 16
+
+
+def test_l2_note_tells_apart_workloads_that_exceed_l2():
+    assert "exceeds L2" in bench.l2_note(bench.workload_info("prenorm_block_f32"))
+    assert "exceeds L2" in bench.l2_note(bench.workload_info("linear_bn_swish_f32"))
+    assert "fits in L2" in bench.l2_note(bench.workload_info("conv1d_groupnorm_f32"))
+
+
+def test_json_line_assembly_with_a_stubbed_gpu_arm(monkeypatch, capsys):
+    """main() on one rank with the GPU arm replaced by fixed numbers: the line
+    carries the contract's keys, and value/bandwidth follow from them."""
+    import json
+    import sys
+    info = bench.workload_info("prenorm_block_f32")
+    fake = dict(value=430.0, ms_per_step=0.12, steps=100, launches=200,
+                roofline=dict(bound="tensor", achieved=430.0, peak=963.2, unit="TFLOP/s",
+                              frac=0.446, traffic=None),
+                kernels={}, clocks=dict(sm_mhz=2070.0, sm_max_mhz=2070.0, reasons=[]),
+                info=info, step_ms_p10=0.119, step_ms_p90=0.121,
+                e2e=dict(value=50.0, unit="TFLOP/s", h2d_bytes_per_step=1,
+                         d2h_bytes_per_step=1))
+    monkeypatch.setattr(bench, "gpu_arm", lambda args, world, rank, local: fake)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--no-cpu-baseline", "--steps", "100"])
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    bench.main()
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "gpu_launches", "clocks", "bandwidth"):
+        assert key in line, key
+    assert line["n_gpus"] == 1 and line["value"] == 430.0 and line["warmup"] >= 3
+    assert line["config"]["workload"] == "prenorm_block_f32"
+    assert line["bandwidth"]["value"] == pytest.approx(info["min_bytes"] / 0.12e-3 / 1e9, abs=0.1)
