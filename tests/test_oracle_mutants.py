@@ -35,6 +35,12 @@ MUTANTS = {
     "divide dropped": ("double u = (v + add_bias) / divide_value;", "double u = (v + add_bias);"),
     "sigmoid sign": ("return 1.0 / (1.0 + exp(-u));", "return 1.0 / (1.0 + exp(u));"),
     "bn train uses running stats": ("mu = s / B;", "mu = running_mean ? running_mean[j] : s / B;"),
+    "gn stride ignored in the taps": ("const int s = t * stride - padding + k * dilation;",
+                                     "const int s = t - padding + k * dilation;"),
+    "gn dilation ignored in the taps": ("const int s = t * stride - padding + k * dilation;",
+                                       "const int s = t * stride - padding + k;"),
+    "gn conv bias dropped": ("for (int t = 0; t < To; ++t) yrow[t] = bias ? bias[o] : 0.0;",
+                             "for (int t = 0; t < To; ++t) yrow[t] = 0.0;"),
     "block train: running var biased": ("momentum * var * cnt / (cnt - 1.0);", "momentum * var;"),
     "block train: unbiased var normalizes": ("const double var = ss / cnt;",
                                              "const double var = ss / (cnt - 1.0);"),
@@ -60,7 +66,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, ORACLE_LIB_OVERRIDE=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_oracle_block.py", "tests/test_oracle_block_train.py",
-                        "tests/test_oracle_gn.py",
+                        "tests/test_oracle_gn.py", "tests/test_oracle_properties.py",
                         "tests/test_oracle_linear.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"mutant '{name}' survived the pins:\n{r.stdout[-2000:]}"
