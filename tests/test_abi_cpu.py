@@ -182,6 +182,17 @@ def test_binding_fails_loudly_without_gpu():
                                      inp.beta, inp.eps, inp.weight, inp.bias, inp.dilation)
 
 
+def test_train_binding_fails_loudly_without_gpu():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from normalization_convolution_blocks_gb300 import api, synthetic
+    inp = synthetic.prenorm_block_inputs(2, 16, 32, 2)
+    with pytest.raises(RuntimeError):
+        api.prenorm_dilconv_residual_train(inp.x, None, None, inp.gamma, inp.beta, inp.eps, 0.1,
+                                           inp.weight, inp.bias, inp.dilation)
+
+
 def _host(lib, **kw):
     a = dict(x=FAKE, out=FAKE2, dt=0, N=4, C=32, L=64, k=3, d=4, pad=4, rm=FAKE, rv=FAKE,
              g=FAKE, b=FAKE, eps=1e-5, w=FAKE, bias=FAKE, chunk=2, ws=ctypes.c_void_p(0x30000000),
