@@ -23,6 +23,8 @@
  *   (out_features, in_features) with in_features fastest.
  * - The library never allocates.  Scratch space is the caller's `workspace`
  *   (device memory, 256-byte aligned, at least *_workspace_size() bytes).
+ *   One exception: nrc_prenorm_dilconv_residual_noalloc keeps its scratch in
+ *   a fixed library-owned device array instead (see its block below).
  * - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
  *   is the legacy default stream).  No call synchronises the host.  The
  *   workspace and outputs must not be reused until the stream has passed the
@@ -179,11 +181,16 @@ nrc_status nrc_prenorm_dilconv_residual_host(
  * Limit: the array is nrc_prenorm_dilconv_residual_noalloc_max_bytes() (4 MiB),
  * present on every GPU that loads the library until the process exits; it
  * holds fp32 C <= 512 or bf16 C <= 768.  Larger C returns NRC_ERR_WORKSPACE.
+ * Argument errors are checked first and return the same codes as
+ * nrc_prenorm_dilconv_residual; the size limit is checked next; no CUDA call
+ * is made before both pass.
  * The first call on a device looks up the array's device address (one
- * cudaGetSymbolAddress, with that device current); make that first call before
- * any stream capture.  All calls share the array and each rewrites what it
- * uses, so nothing needs clearing, but calls that overlap on the GPU (several
- * streams or host threads at once) race on it.
+ * cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  cudaDeviceReset() on a device makes
+ * the cached address stale: do not use this entry point on that device after
+ * a reset.  All calls share the array and each rewrites what it uses, so
+ * nothing needs clearing, but calls that overlap on the GPU (several streams
+ * or host threads at once) race on it.
  * ------------------------------------------------------------------------ */
 size_t nrc_prenorm_dilconv_residual_noalloc_max_bytes(void);
 

@@ -412,6 +412,30 @@ def prenorm_dilconv_residual_noalloc(x, bn_running_mean, bn_running_var, bn_gamm
     this binding allocates nothing either.  Calls that overlap on the GPU race
     on the shared scratch."""
     lib = load()
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be float32 or bfloat16")
+    if x.dim() != 3:
+        raise ValueError("x must be (N, C, L)")
+    if out is None or out.shape != x.shape or out.dtype != x.dtype:
+        raise ValueError("out must be given with x's shape and dtype")
+    dev = x.device
+    for name, t, dtype in (("x", x, x.dtype), ("out", out, x.dtype),
+                           ("bn_running_mean", bn_running_mean, torch.float32),
+                           ("bn_running_var", bn_running_var, torch.float32),
+                           ("bn_gamma", bn_gamma, torch.float32),
+                           ("bn_beta", bn_beta, torch.float32),
+                           ("conv_weight", conv_weight, x.dtype),
+                           ("conv_bias", conv_bias, x.dtype)):
+        if t is None:
+            if name == "conv_bias":
+                continue
+            raise ValueError(f"{name} is required")
+        if not t.is_cuda or t.device != dev:
+            raise ValueError(f"{name} must be on x's device ({dev})")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
     dt = NRC_F32 if x.dtype == torch.float32 else NRC_BF16
     N, C, L = x.shape
     padding = dilation if padding is None else padding

@@ -1177,20 +1177,31 @@ nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int 
         "prenorm_block_gemm", p, pl.g, st);
 }
 
-// Shared argument checks of the block entry points (device or host buffers).
-nrc_status block_check(const void* x, const void* out, nrc_dtype dt, int N, int C, int L,
-                       int kernel_size, int dilation, int padding, const void* rm,
-                       const void* rv, const void* gamma, const void* beta, float bn_eps,
-                       const void* conv_weight, const void* workspace) {
+// Shared argument checks of the block entry points (device or host buffers),
+// except the workspace pointer (the allocation-free entry point has none).
+nrc_status block_check_args(const void* x, const void* out, nrc_dtype dt, int N, int C, int L,
+                            int kernel_size, int dilation, int padding, const void* rm,
+                            const void* rv, const void* gamma, const void* beta, float bn_eps,
+                            const void* conv_weight) {
     if (dt != NRC_F32 && dt != NRC_BF16) return NRC_ERR_INVALID_ARG;
-    if (!x || !out || !rm || !rv || !gamma || !beta || !conv_weight || !workspace)
-        return NRC_ERR_INVALID_ARG;
+    if (!x || !out || !rm || !rv || !gamma || !beta || !conv_weight) return NRC_ERR_INVALID_ARG;
     if (N <= 0 || C <= 0 || L <= 0 || dilation <= 0 || padding < 0) return NRC_ERR_INVALID_ARG;
     if (!(bn_eps >= 0.f) || !std::isfinite(bn_eps)) return NRC_ERR_INVALID_ARG;
     if (kernel_size != 3 || padding != dilation) return NRC_ERR_UNSUPPORTED;
     if (C > 2048) return NRC_ERR_UNSUPPORTED;
     const size_t bytes = (size_t)N * C * L * (dt == NRC_F32 ? 4 : 2);
     if (ranges_overlap(x, bytes, out, bytes)) return NRC_ERR_INVALID_ARG;
+    return NRC_OK;
+}
+
+nrc_status block_check(const void* x, const void* out, nrc_dtype dt, int N, int C, int L,
+                       int kernel_size, int dilation, int padding, const void* rm,
+                       const void* rv, const void* gamma, const void* beta, float bn_eps,
+                       const void* conv_weight, const void* workspace) {
+    const nrc_status s = block_check_args(x, out, dt, N, C, L, kernel_size, dilation, padding,
+                                          rm, rv, gamma, beta, bn_eps, conv_weight);
+    if (s != NRC_OK) return s;
+    if (!workspace) return NRC_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return NRC_ERR_ALIGNMENT;
     return NRC_OK;
 }
@@ -1549,7 +1560,9 @@ void* g_noalloc_addr[64];   // device address of g_noalloc_scratch, per device
 
 // Device address of the scratch array on the current device.  The name of a
 // __device__ array in host code is only a host-side stand-in, so the address
-// is looked up (once per device, with that device current).
+// is looked up (once per device, with that device current) and cached.  A
+// cudaDeviceReset() on the device unloads the module and makes the cached
+// address stale: the entry point must not be used on that device afterwards.
 nrc_status noalloc_scratch_address(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NRC_ERR_CUDA;
@@ -1573,7 +1586,11 @@ extern "C" nrc_status nrc_prenorm_dilconv_residual_noalloc(
     const void* x, void* out, nrc_dtype dt, int N, int C, int L, int kernel_size, int dilation,
     int padding, const float* rm, const float* rv, const float* gamma, const float* beta,
     float bn_eps, const void* conv_weight, const void* conv_bias, void* stream) {
-    if ((dt != NRC_F32 && dt != NRC_BF16) || C <= 0) return NRC_ERR_INVALID_ARG;
+    // The same argument checks (and status codes) as the workspace entry point
+    // come first; then the array's size limit; only then any CUDA call.
+    const nrc_status c = block_check_args(x, out, dt, N, C, L, kernel_size, dilation, padding,
+                                          rm, rv, gamma, beta, bn_eps, conv_weight);
+    if (c != NRC_OK) return c;
     if (nrc_prenorm_dilconv_residual_workspace_size(C, dt) > kNoAllocScratchBytes)
         return NRC_ERR_WORKSPACE;
     void* scratch = nullptr;

@@ -228,3 +228,28 @@ def test_host_buffer_workspace_query(lib):
     assert f(32, 256, 4096, 0, 64) == f(32, 256, 4096, 0, 32)      # chunk capped at N
     assert f(32, 256, 4096, 1, 4) < four                          # bf16 halves the buffers
     assert f(0, 256, 4096, 0, 4) == 0 and f(32, 256, 4096, 0, 0) == 0 and f(4, 8, 8, 9, 1) == 0
+
+
+def _noalloc(lib, **kw):
+    a = dict(x=FAKE, out=FAKE2, dt=0, N=2, C=32, L=64, k=3, d=4, pad=4, rm=FAKE, rv=FAKE,
+             g=FAKE, b=FAKE, eps=1e-5, w=FAKE, bias=FAKE, stream=None)
+    a.update(kw)
+    return lib.nrc_prenorm_dilconv_residual_noalloc(
+        a["x"], a["out"], a["dt"], a["N"], a["C"], a["L"], a["k"], a["d"], a["pad"], a["rm"],
+        a["rv"], a["g"], a["b"], a["eps"], a["w"], a["bias"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), 1), (dict(out=None), 1), (dict(w=None), 1), (dict(dt=7), 1),
+    (dict(N=0), 1), (dict(eps=float("nan")), 1), (dict(k=5), 2), (dict(pad=3), 2),
+    (dict(out=ctypes.c_void_p(0x10000000 + 64)), 1),          # out overlaps x
+    # the argument checks come before the array's size limit: the same codes as
+    # the workspace entry point even when C is too large for the array
+    (dict(x=None, C=640), 1), (dict(w=None, C=1024), 1), (dict(C=4096), 2),
+    (dict(C=640), 4),                                          # fp32 C=640 exceeds 4 MiB
+    (dict(C=1024, dt=1), 4),                                   # bf16 C=1024 too
+])
+def test_noalloc_validation_order(lib, kw, expect):
+    """The allocation-free entry rejects bad arguments with the workspace entry
+    point's codes, then sizes beyond its array, before any CUDA call."""
+    assert _noalloc(lib, **kw) == expect
