@@ -8,8 +8,8 @@
  *       out = x + Conv1d(ReLU(BatchNorm1d_eval(x))), kernel_size 3,
  *       padding = dilation (so the output length equals L), C_in = C_out.
  *   nrc_conv1d_groupnorm           "FW-GLM-5-1 l2_p35", problem analysis:
- *       Conv1d(C_in -> C_out, kernel_size 3, stride 1, padding 1, dilation 1,
- *       bias optional) followed by GroupNorm(num_groups, C_out, eps, affine).
+ *       Conv1d(C_in -> C_out, kernel_size, stride, padding, dilation, bias
+ *       optional) followed by GroupNorm(num_groups, C_out, eps, affine).
  *   nrc_linear_bn_swish            "Kimi-K2.6 l2_p97", problem statement:
  *       Linear(in, out) -> BatchNorm1d(out) (training: batch statistics and
  *       running-stat update; eval: running statistics) -> + scalar bias ->
@@ -203,23 +203,36 @@ nrc_status nrc_prenorm_dilconv_residual_noalloc(
 
 /* ------------------------------------------------------------------------
  * Conv1d + GroupNorm ("FW-GLM-5-1 l2_p35", problem analysis and its
- * normalisation kernel)
+ * normalisation kernel; the module's constructor takes kernel_size, stride,
+ * padding, dilation, eps and affine)
  *
- *   y[n,o,t] = bias[o] + sum_c sum_k W[o,c,k] * x[n, c, t - 1 + k]   (x = 0 outside)
+ *   T_out    = floor((T + 2*padding - dilation*(kernel_size - 1) - 1) / stride) + 1
+ *   y[n,o,t] = bias[o] + sum_c sum_k W[o,c,k] * x[n, c, t*stride - padding + k*dilation]
+ *              (x = 0 outside [0, T)),  0 <= t < T_out
  *   group g = o / (C_out / num_groups)
  *   mu, var  = mean and biased variance of y over the group's channels and all t
  *   out      = (y - mu) / sqrt(var + eps) * gamma[o] + beta[o]
  *
- * x: (N, C_in, T) fp32.  out: (N, C_out, T) fp32, must not overlap x; it also
- * holds y between the two kernels of the call.
- * conv_weight: (C_out, C_in, 3) fp32.  conv_bias: (C_out) or NULL.
+ * x: (N, C_in, T) fp32.  out: (N, C_out, T_out) fp32, must not overlap x; when
+ * the tiles do not fit one wave of resident CTAs it also holds y between the
+ * call's two kernels.
+ * conv_weight: (C_out, C_in, kernel_size) fp32.  conv_bias: (C_out) or NULL.
  * gn_gamma, gn_beta: (C_out) fp32, both NULL for affine=False.
- * kernel_size 3, stride 1, padding 1, dilation 1 only (else UNSUPPORTED).
+ * kernel_size >= 1, stride >= 1, padding >= 0, dilation >= 1 and T_out >= 1
+ * (else INVALID_ARG); kernel_size <= 64 (else UNSUPPORTED).
  * C_out % num_groups == 0 (else INVALID_ARG); when C_out > 256 the group
  * size must divide 256 (else UNSUPPORTED).
+ * workspace: >= nrc_conv1d_groupnorm_workspace_size(...) bytes with the same
+ * shape and conv arguments (0 from the query: invalid arguments).
  * ------------------------------------------------------------------------ */
+
+/* T_out of the conv above, or 0 when the arguments are invalid or the kernel
+ * does not fit the padded input. */
+int nrc_conv1d_output_length(int T, int kernel_size, int stride, int padding, int dilation);
+
 size_t nrc_conv1d_groupnorm_workspace_size(int N, int C_in, int C_out, int T,
-                                           int num_groups);
+                                           int kernel_size, int stride, int padding,
+                                           int dilation, int num_groups);
 
 nrc_status nrc_conv1d_groupnorm(
     const float *x, float *out, int N, int C_in, int C_out, int T,
@@ -275,6 +288,16 @@ int nrc_last_error_site(void);
 /* Limit of every device-side wait, in nanoseconds (default 2e9).  Applies to
  * launches made after the call. */
 void nrc_set_wait_timeout_ns(uint64_t ns);
+
+/* Limit of ONE wait site only: the grid-wide barrier of the one-wave
+ * Conv1d + GroupNorm kernel (wait site 9), where every CTA has finished its
+ * copies and MMAs before it waits.  ns = 0 returns that site to the general
+ * limit above.  A wait that gives up there records NRC_ERR_TIMEOUT (site 9),
+ * and the CTA returns without normalising its tile; the next call, made with
+ * the limit restored, is unaffected.  This exists to exercise a real kernel's
+ * give-up path; every other wait keeps the general limit.  Applies to
+ * launches made after the call. */
+void nrc_set_grid_barrier_timeout_ns(uint64_t ns);
 
 /* Fault-path self test: launches one CTA whose thread waits, with the given
  * limit, on an mbarrier that nothing ever arrives at.  The wait gives up and

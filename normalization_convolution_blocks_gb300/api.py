@@ -64,13 +64,15 @@ def load() -> ctypes.CDLL:
         "nrc_prenorm_dilconv_residual_noalloc_max_bytes": ([], sz),
         "nrc_prenorm_dilconv_residual_noalloc": ([p, p, i, i, i, i, i, i, i, p, p, p, p, f, p, p,
                                                   p], i),
-        "nrc_conv1d_groupnorm_workspace_size": ([i, i, i, i, i], sz),
+        "nrc_conv1d_output_length": ([i, i, i, i, i], i),
+        "nrc_conv1d_groupnorm_workspace_size": ([i, i, i, i, i, i, i, i, i], sz),
         "nrc_conv1d_groupnorm": ([p, p, i, i, i, i, i, i, i, i, p, p, i, p, p, f, p, sz, p], i),
         "nrc_linear_bn_swish_workspace_size": ([i, i, i], sz),
         "nrc_linear_bn_swish": ([p, p, i, i, i, p, p, p, p, p, p, p, f, f, i, p, f, p, sz, p], i),
         "nrc_query_status": ([p], i),
         "nrc_last_error_site": ([], i),
         "nrc_set_wait_timeout_ns": ([u64], None),
+        "nrc_set_grid_barrier_timeout_ns": ([u64], None),
         "nrc_selftest_wait_timeout": ([u64, p], i),
         "nrc_trace_enable": ([i], None),
         "nrc_trace_count": ([], i),
@@ -277,14 +279,22 @@ def _keep_alive(stream, *tensors):
 # ---------------------------------------------------------------------------
 # Conv1d + GroupNorm
 # ---------------------------------------------------------------------------
-def conv1d_groupnorm_workspace_size(N, C_in, C_out, T, num_groups) -> int:
-    return int(load().nrc_conv1d_groupnorm_workspace_size(N, C_in, C_out, T, num_groups))
+def conv1d_output_length(T, kernel_size=3, stride=1, padding=1, dilation=1) -> int:
+    """T_out of Conv1d(kernel_size, stride, padding, dilation) on T positions (0 if invalid)."""
+    return int(load().nrc_conv1d_output_length(T, kernel_size, stride, padding, dilation))
+
+
+def conv1d_groupnorm_workspace_size(N, C_in, C_out, T, num_groups, kernel_size=3, stride=1,
+                                    padding=1, dilation=1) -> int:
+    return int(load().nrc_conv1d_groupnorm_workspace_size(N, C_in, C_out, T, kernel_size, stride,
+                                                          padding, dilation, num_groups))
 
 
 def conv1d_groupnorm(x, conv_weight, conv_bias, num_groups, gn_gamma, gn_beta, eps=1e-5,
-                     kernel_size=3, stride=1, padding=1, dilation=1, out=None, workspace=None,
+                     kernel_size=None, stride=1, padding=1, dilation=1, out=None, workspace=None,
                      stream=None):
-    """GroupNorm(num_groups)(Conv1d(x)); x (N, C_in, T) fp32, conv_weight (C_out, C_in, 3)."""
+    """GroupNorm(num_groups)(Conv1d(x)); x (N, C_in, T) fp32, conv_weight
+    (C_out, C_in, kernel_size); the result is (N, C_out, T_out)."""
     lib = load()
     host = not x.is_cuda
     dev = _target_device(x)
@@ -292,10 +302,20 @@ def conv1d_groupnorm(x, conv_weight, conv_bias, num_groups, gn_gamma, gn_beta, e
     N, Cin, T = xd.shape
     w = _dev(conv_weight, dev, torch.float32)
     Cout = w.shape[0]
+    if kernel_size is None:
+        kernel_size = w.shape[2]
+    if w.dim() != 3 or w.shape[1] != Cin or w.shape[2] != kernel_size:
+        raise ValueError("conv_weight must be (C_out, C_in, kernel_size)")
+    T_out = int(lib.nrc_conv1d_output_length(T, kernel_size, stride, padding, dilation))
+    if T_out <= 0:
+        raise ValueError("the conv's kernel does not fit the padded input")
     cb, g, b = (_dev(t, dev, torch.float32) for t in (conv_bias, gn_gamma, gn_beta))
-    o = out if (out is not None and not host) else torch.empty((N, Cout, T), device=dev,
+    o = out if (out is not None and not host) else torch.empty((N, Cout, T_out), device=dev,
                                                                 dtype=torch.float32)
-    ws = _workspace(lib.nrc_conv1d_groupnorm_workspace_size(N, Cin, Cout, T, num_groups), dev,
+    if o.shape != (N, Cout, T_out) or o.dtype != torch.float32 or not o.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 (N, C_out, T_out) tensor")
+    ws = _workspace(lib.nrc_conv1d_groupnorm_workspace_size(N, Cin, Cout, T, kernel_size, stride,
+                                                            padding, dilation, num_groups), dev,
                     workspace)
     st = lib.nrc_conv1d_groupnorm(_ptr(xd), _ptr(o), N, Cin, Cout, T, kernel_size, stride,
                                   padding, dilation, _ptr(w), _ptr(cb), num_groups, _ptr(g),
@@ -371,6 +391,11 @@ def last_error_site() -> int:
 
 def set_wait_timeout_ns(ns: int) -> None:
     load().nrc_set_wait_timeout_ns(int(ns))
+
+
+def set_grid_barrier_timeout_ns(ns: int) -> None:
+    """Limit of the one-wave GroupNorm kernel's grid barrier only (0: the general limit)."""
+    load().nrc_set_grid_barrier_timeout_ns(int(ns))
 
 
 def selftest_wait_timeout(limit_ns: int, stream=None) -> None:

@@ -21,6 +21,9 @@ int g_sm_count[kMaxDevices];
 int g_coop[kMaxDevices];         // 0 unknown, 1 supported, 2 not
 std::mutex g_mu;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+// Limit of the one-wave GroupNorm kernel's grid-wide barrier only; 0: the
+// general limit.
+std::atomic<unsigned long long> g_grid_barrier_timeout_ns{0ull};
 int g_last_site = 0;
 
 int current_device() {
@@ -43,6 +46,11 @@ int* device_status_ptr() {
 }
 
 unsigned long long wait_timeout_ns() { return g_timeout_ns.load(); }
+
+unsigned long long grid_barrier_timeout_ns() {
+    const unsigned long long v = g_grid_barrier_timeout_ns.load();
+    return v ? v : g_timeout_ns.load();
+}
 
 int device_sm_count() {
     const int d = current_device();
@@ -181,6 +189,10 @@ extern "C" int nrc_version(void) { return 100; }
 
 extern "C" void nrc_set_wait_timeout_ns(uint64_t ns) {
     g_timeout_ns.store(ns > 0 ? (unsigned long long)ns : 1ull);
+}
+
+extern "C" void nrc_set_grid_barrier_timeout_ns(uint64_t ns) {
+    g_grid_barrier_timeout_ns.store((unsigned long long)ns);
 }
 
 extern "C" int nrc_last_error_site(void) { return g_last_site; }

@@ -3,7 +3,9 @@
 //     ("Kimi-K2.6 l2_p12", problem statement)
 //   * Conv1d(k=3, pad=1) + GroupNorm ("FW-GLM-5-1 l2_p35", problem analysis)
 //
-// GEMM view of one sample n: D[t][o] = sum_tap sum_c z[c][t - pad + tap*dil] * W[o][c][tap].
+// GEMM view of one sample n: D[t][o] = sum_tap sum_c z[c][t*stride - pad + tap*dil] * W[o][c][tap]
+// (the block: stride 1, three taps, pad = dil; Conv1d + GroupNorm: any kernel
+// size, stride, padding and dilation).
 // Tile rows are 128 consecutive t, tile columns BN output channels; the K loop
 // runs over (tap, 64-channel chunk).  The A operand (activations) is produced
 // in tensor memory by the prologue warps: the conv input for the tile's shifted
@@ -56,8 +58,10 @@ struct ConvParams {
     CUtensorMap xmap;       // x as (L, Cin, N) boxes of (128 + 16/esize) x 64 x 1 (staged A)
     const void* x;          // (N, Cin, L)
     void* out;              // (N, Cout, L)
-    int N, Cin, Cout, L;
-    int pad, dil;           // tap k of output t reads t - pad + k*dil
+    int N, Cin, Cout, L;    // L: output length (tile rows, out rows)
+    int Lin;                // input length (rows of x); the block has Lin == L
+    int pad, dil, stride;   // tap k of output t reads t*stride - pad + k*dil
+    int ksz;                // taps of the kernel (3 for the block)
     int n_tt, n_ot, n_chunks, n_kiters, BN;
     // eval-mode BatchNorm of the block's prologue (NULL rm: no BN/ReLU)
     const float *rm, *rv, *gamma, *beta;
@@ -119,15 +123,15 @@ __device__ __forceinline__ ConvTile conv_tile(const ConvParams& p, int tile) {
     return r;
 }
 
-// One 16-byte chunk of the weight image: W (Cout, Cin, 3) -> for each (o tile,
+// One 16-byte chunk of the weight image: W (Cout, Cin, ksz) -> for each (o tile,
 // tap, 64-channel chunk) the B-stage image, NP parts of BN rows x 64 bf16,
 // 128B-swizzled (fp32 split into hi + lo bf16; bf16 copied).  Rows past Cout
 // and channels past Cin are zero.  idx enumerates (o tile, K stage, row, chunk).
 template <typename T, int NP>
 __device__ __forceinline__ void pack_conv_chunk(const T* __restrict__ w,
                                                 uint8_t* __restrict__ pack, int Cout, int Cin,
-                                                int BN, int n_chunks, size_t idx) {
-    const int n_kiters = 3 * n_chunks;
+                                                int BN, int n_chunks, int ksz, size_t idx) {
+    const int n_kiters = ksz * n_chunks;
     const int j = (int)(idx & 7);
     size_t rest = idx >> 3;
     const int row = (int)(rest % BN);
@@ -141,7 +145,7 @@ __device__ __forceinline__ void pack_conv_chunk(const T* __restrict__ w,
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const int c = c0 + e;
-        v[e] = (o < Cout && c < Cin) ? load_f<T>(w + ((size_t)o * Cin + c) * 3 + tap) : 0.f;
+        v[e] = (o < Cout && c < Cin) ? load_f<T>(w + ((size_t)o * Cin + c) * ksz + tap) : 0.f;
     }
     const size_t blk = ((size_t)ot * n_kiters + kiter) * NP;
     const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)j);
@@ -317,7 +321,7 @@ struct ConvProblem {
             for (size_t idx = (size_t)blockIdx.x * nthr + tid; idx < units;
                  idx += (size_t)gridDim.x * nthr)
                 pack_conv_chunk<T, NP>(static_cast<const T*>(p.w_raw), p.wpack_out, p.Cout,
-                                       p.Cin, p.BN, p.n_chunks, idx);
+                                       p.Cin, p.BN, p.n_chunks, p.ksz, idx);
             fence_proxy_async_global();
             __threadfence();
         }
@@ -355,12 +359,19 @@ struct ConvProblem {
         }
     }
 
+    // K stage -> (tap, 64-channel chunk): taps outermost.
+    static __device__ __forceinline__ void stage_tap(const Params& p, int kiter, int& tap,
+                                                     int& chunk) {
+        tap = kiter / p.n_chunks;
+        chunk = kiter - tap * p.n_chunks;
+    }
+
     // Input position read by tap `tap` for output row t, and the channel base.
     static __device__ __forceinline__ void where(const Params& p, const Tile& tl, int kiter,
                                                  int row, int k0, int& s, int& c0) {
-        const int tap = kiter >= 2 * p.n_chunks ? 2 : (kiter >= p.n_chunks ? 1 : 0);
-        const int chunk = kiter - tap * p.n_chunks;
-        s = tl.tt * kBM + row - p.pad + tap * p.dil;
+        int tap, chunk;
+        stage_tap(p, kiter, tap, chunk);
+        s = (tl.tt * kBM + row) * p.stride - p.pad + tap * p.dil;
         c0 = chunk * kBK + k0;
     }
 
@@ -368,15 +379,15 @@ struct ConvProblem {
                                                   int row, int k0, float (&v)[32]) {
         int s, c0;
         where(p, tl, kiter, row, k0, s, c0);
-        if ((unsigned)s < (unsigned)p.L) {
-            const T* xp = static_cast<const T*>(p.x) + ((size_t)tl.n * p.Cin + c0) * p.L + s;
+        if ((unsigned)s < (unsigned)p.Lin) {
+            const T* xp = static_cast<const T*>(p.x) + ((size_t)tl.n * p.Cin + c0) * p.Lin + s;
             if (c0 + 32 <= p.Cin) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = load_f<T>(xp + (size_t)i * p.L);
+                for (int i = 0; i < 32; ++i) v[i] = load_f<T>(xp + (size_t)i * p.Lin);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    v[i] = (c0 + i < p.Cin) ? load_f<T>(xp + (size_t)i * p.L) : 0.f;
+                    v[i] = (c0 + i < p.Cin) ? load_f<T>(xp + (size_t)i * p.Lin) : 0.f;
             }
         } else {
 #pragma unroll
@@ -384,7 +395,7 @@ struct ConvProblem {
         }
     }
 
-    // Staged A.  Tile rows t0 .. t0+128 read input rows from
+    // Staged A (stride 1 only).  Tile rows t0 .. t0+128 read input rows from
     // s = t0 - pad + tap*dil on; the stage's box starts at s rounded down to the
     // 16-byte boundary and row r sits at offset r + s mod kAlign.  Rows outside
     // [0, L) and channels past Cin come back as the map's fill: NaN when BN
@@ -396,8 +407,8 @@ struct ConvProblem {
 
     static __device__ __forceinline__ void issue_a_box(const Params& p, const Tile& tl,
                                                        int kiter, uint32_t dst, uint32_t bar) {
-        const int tap = kiter >= 2 * p.n_chunks ? 2 : (kiter >= p.n_chunks ? 1 : 0);
-        const int chunk = kiter - tap * p.n_chunks;
+        int tap, chunk;
+        stage_tap(p, kiter, tap, chunk);
         const int s = box_row0(p, tl, tap);
         tma_load_3d(dst, &p.xmap, s & ~(kAlign - 1), chunk * kBK, tl.n, bar);
     }
@@ -405,8 +416,8 @@ struct ConvProblem {
     static __device__ __forceinline__ void read_a(const Params& p, const uint8_t* extra,
                                                   const Tile& tl, int kiter, int row, int k0,
                                                   int lane, uint32_t box, float (&v)[32]) {
-        const int tap = kiter >= 2 * p.n_chunks ? 2 : (kiter >= p.n_chunks ? 1 : 0);
-        const int chunk = kiter - tap * p.n_chunks;
+        int tap, chunk;
+        stage_tap(p, kiter, tap, chunk);
         const int rem = box_row0(p, tl, tap) & (kAlign - 1);
         const uint32_t a = box + (uint32_t)((k0 * kBoxW + row + rem) * (int)sizeof(T));
 #pragma unroll
@@ -437,7 +448,7 @@ struct ConvProblem {
         if (p.rm == nullptr) return;                   // plain conv input
         int s, c0;
         where(p, tl, kiter, row, k0, s, c0);
-        if ((unsigned)s >= (unsigned)p.L) return;      // padding applies to z, after BN+ReLU
+        if ((unsigned)s >= (unsigned)p.Lin) return;    // padding applies to z, after BN+ReLU
         const float4* sc = reinterpret_cast<const float4*>(extra) + c0 / 4;
         const float4* sh = reinterpret_cast<const float4*>(extra) + (p.n_chunks * kBK + c0) / 4;
 #pragma unroll
@@ -892,19 +903,20 @@ struct ConvProblem {
 };
 
 // ---------------------------------------------------------------------------
-// Weight repack: W (Cout, Cin, 3) -> for each (o tile, tap, 64-channel chunk)
+// Weight repack: W (Cout, Cin, ksz) -> for each (o tile, tap, 64-channel chunk)
 // the B-stage image: NP parts of BN rows x 64 bf16, 128B-swizzled.  fp32
 // weights are split into hi + lo bf16 parts; bf16 weights are copied.  Rows
 // past Cout and channels past Cin are zero.  One thread per 16-byte chunk.
 // ---------------------------------------------------------------------------
 template <typename T, int NP>
 __global__ void pack_conv_weight_kernel(const T* __restrict__ w, uint8_t* __restrict__ pack,
-                                        int Cout, int Cin, int BN, int n_ot, int n_chunks) {
+                                        int Cout, int Cin, int BN, int n_ot, int n_chunks,
+                                        int ksz) {
     griddep_launch_dependents();       // the GEMM may launch; it waits before reading B
-    const size_t total = (size_t)n_ot * 3 * n_chunks * BN * 8;   // 16-byte chunks per part
+    const size_t total = (size_t)n_ot * ksz * n_chunks * BN * 8;   // 16-byte chunks per part
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
          idx += (size_t)gridDim.x * blockDim.x)
-        pack_conv_chunk<T, NP>(w, pack, Cout, Cin, BN, n_chunks, idx);
+        pack_conv_chunk<T, NP>(w, pack, Cout, Cin, BN, n_chunks, ksz, idx);
 }
 
 // ---------------------------------------------------------------------------
@@ -999,7 +1011,7 @@ struct ConvPlan {
 // Extra shared memory: BN fold (scale, shift) when present, the staged bias,
 // then (128-byte aligned) stage_bytes for the epilogue's chunk buffers.
 static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn,
-                          uint32_t x_box_bytes = 0, uint32_t stage_bytes = 0) {
+                          uint32_t x_box_bytes = 0, uint32_t stage_bytes = 0, int ksz = 3) {
     ConvPlan pl{};
     const int BN = Cout <= 256 ? ((Cout + 15) / 16) * 16 : 256;
     pl.n_ot = ceil_div(Cout, BN);
@@ -1010,7 +1022,7 @@ static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn,
                                (uint32_t)((pl.n_ot * BN + 32) * 4);
     pl.stage_off = (int)((fold_bias + 127u) & ~127u);
     const uint32_t extra = stage_bytes ? (uint32_t)pl.stage_off + stage_bytes : fold_bias;
-    pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), 3 * pl.n_chunks, NP,
+    pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), ksz * pl.n_chunks, NP,
                           extra, x_box_bytes);
     pl.wpack_bytes = (size_t)pl.n_ot * pl.g.num_kiters * NP * BN * 128;
     return pl;
@@ -1031,13 +1043,14 @@ static bool make_x_map(ConvParams& p, const void* x, int N, int Cin, int L, bool
         dims, strides, box, nan_fill);
 }
 
-// Plans the conv GEMM, staged when x allows it and the slots fit; fills the
-// map and returns whether the staged kernel runs.  p.x and p.out must be set:
-// the staged bf16 residual epilogue moves x and out in 8-byte words, so it
-// also needs out 8-byte aligned (x is 16-byte aligned for the map).
+// Plans the conv GEMM (L output rows, Lin input rows, ksz taps), staged when x
+// allows it (stride 1, aligned rows) and the slots fit; fills the map and
+// returns whether the staged kernel runs.  p.x and p.out must be set: the
+// staged bf16 residual epilogue moves x and out in 8-byte words, so it also
+// needs out 8-byte aligned (x is 16-byte aligned for the map).
 template <typename T>
 static bool plan_conv_staged(ConvParams& p, ConvPlan& pl, int N, int Cin, int Cout, int L,
-                             bool with_bn) {
+                             bool with_bn, int Lin, int stride = 1, int ksz = 3) {
     constexpr int NP = sizeof(T) == 4 ? 2 : 1;
     constexpr uint32_t box_bytes = (uint32_t)((kBM + 16 / sizeof(T)) * kBK * sizeof(T));
     // the staged bf16 residual epilogue needs its two chunk buffers, the fused
@@ -1047,14 +1060,14 @@ static bool plan_conv_staged(ConvParams& p, ConvPlan& pl, int N, int Cin, int Co
         (with_bn && sizeof(T) == 2) ? 2u * ConvProblem<T, ConvEpi::kResidual, true>::kChunkBufBytes
                                     : fused_bytes;
     const bool out_ok = !(with_bn && sizeof(T) == 2) || aligned(p.out, 8);
-    if (out_ok && make_x_map<T>(p, p.x, N, Cin, L, with_bn)) {
-        pl = plan_conv(N, Cin, Cout, L, NP, with_bn, box_bytes, stage_bytes);
+    if (out_ok && stride == 1 && make_x_map<T>(p, p.x, N, Cin, Lin, with_bn)) {
+        pl = plan_conv(N, Cin, Cout, L, NP, with_bn, box_bytes, stage_bytes, ksz);
         if (pl.g.b_stages >= 2 && pl.g.x_depth >= 2) {
             p.stage_off = pl.stage_off;
             return true;
         }
     }
-    pl = plan_conv(N, Cin, Cout, L, NP, with_bn, 0, fused_bytes);
+    pl = plan_conv(N, Cin, Cout, L, NP, with_bn, 0, fused_bytes, ksz);
     p.stage_off = pl.stage_off;
     return false;
 }
@@ -1087,11 +1100,11 @@ nrc_status block_pack(const void* conv_weight, nrc_dtype dt, int C, void* wpack,
     if (dt == NRC_F32)
         pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
             static_cast<const float*>(conv_weight), static_cast<uint8_t*>(wpack), C, C, pl.g.BN,
-            pl.n_ot, pl.n_chunks);
+            pl.n_ot, pl.n_chunks, 3);
     else
         pack_conv_weight_kernel<__nv_bfloat16, 1><<<elementwise_grid(units), 256, 0, st>>>(
             static_cast<const __nv_bfloat16*>(conv_weight), static_cast<uint8_t*>(wpack), C, C,
-            pl.g.BN, pl.n_ot, pl.n_chunks);
+            pl.g.BN, pl.n_ot, pl.n_chunks, 3);
     return cuda_status(cudaGetLastError());
 }
 
@@ -1107,14 +1120,17 @@ nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int 
     ConvParams p{};
     p.x = x;
     p.out = out;
-    const bool staged = dt == NRC_F32 ? plan_conv_staged<float>(p, pl, N, C, C, L, true)
-                                      : plan_conv_staged<__nv_bfloat16>(p, pl, N, C, C, L, true);
+    const bool staged = dt == NRC_F32 ? plan_conv_staged<float>(p, pl, N, C, C, L, true, L)
+                                      : plan_conv_staged<__nv_bfloat16>(p, pl, N, C, C, L, true, L);
     p.N = N;
     p.Cin = C;
     p.Cout = C;
     p.L = L;
+    p.Lin = L;
     p.pad = padding;
     p.dil = dilation;
+    p.stride = 1;
+    p.ksz = 3;
     p.n_tt = pl.n_tt;
     p.n_ot = pl.n_ot;
     p.n_chunks = pl.n_chunks;
@@ -1422,10 +1438,45 @@ static size_t gn_partials_offset(const ConvPlan& pl) {
     return (pl.wpack_bytes + 255) & ~(size_t)255;
 }
 
+namespace {
+
+constexpr int kMaxConvTaps = 64;
+
+// Output length of Conv1d (PyTorch's definition):
+// floor((T + 2*padding - dilation*(kernel_size - 1) - 1) / stride) + 1, or 0
+// when the arguments are out of range or the result is not positive.
+long long conv1d_out_len(int T, int kernel_size, int stride, int padding, int dilation) {
+    if (T <= 0 || kernel_size <= 0 || stride <= 0 || padding < 0 || dilation <= 0) return 0;
+    const long long span = (long long)dilation * (kernel_size - 1) + 1;
+    const long long num = (long long)T + 2LL * padding - span;
+    if (num < 0) return 0;
+    return num / stride + 1;
+}
+
+// Position arithmetic of the kernels (t*stride - padding + k*dilation, box
+// starts) is 32-bit: every input position a tap can reach must fit.
+bool conv_positions_fit(int T, int kernel_size, int stride, int padding, int dilation,
+                        long long T_out) {
+    const long long reach = (T_out + kBM) * (long long)stride + (long long)dilation * kernel_size;
+    return reach + padding + T < (1LL << 30);
+}
+
+}  // namespace
+
+extern "C" int nrc_conv1d_output_length(int T, int kernel_size, int stride, int padding,
+                                        int dilation) {
+    const long long t = conv1d_out_len(T, kernel_size, stride, padding, dilation);
+    return t > 0 && t < (1LL << 30) ? (int)t : 0;
+}
+
 extern "C" size_t nrc_conv1d_groupnorm_workspace_size(int N, int C_in, int C_out, int T,
-                                                      int num_groups) {
-    if (N <= 0 || C_in <= 0 || C_out <= 0 || T <= 0 || num_groups <= 0) return 0;
-    const ConvPlan pl = plan_conv(N, C_in, C_out, T, 2, false);
+                                                      int kernel_size, int stride, int padding,
+                                                      int dilation, int num_groups) {
+    if (N <= 0 || C_in <= 0 || C_out <= 0 || num_groups <= 0) return 0;
+    if (kernel_size > kMaxConvTaps) return 0;
+    const int T_out = nrc_conv1d_output_length(T, kernel_size, stride, padding, dilation);
+    if (T_out <= 0) return 0;
+    const ConvPlan pl = plan_conv(N, C_in, C_out, T_out, 2, false, 0, 0, kernel_size);
     return gn_partials_offset(pl) + (size_t)N * num_groups * pl.n_tt * kBM * sizeof(float2);
 }
 
@@ -1439,18 +1490,26 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     if (!x || !out || !conv_weight || !workspace) return NRC_ERR_INVALID_ARG;
     if (N <= 0 || C_in <= 0 || C_out <= 0 || T <= 0 || num_groups <= 0)
         return NRC_ERR_INVALID_ARG;
+    if (kernel_size <= 0 || stride <= 0 || padding < 0 || dilation <= 0)
+        return NRC_ERR_INVALID_ARG;
     if ((gn_gamma == nullptr) != (gn_beta == nullptr)) return NRC_ERR_INVALID_ARG;
     if (C_out % num_groups != 0) return NRC_ERR_INVALID_ARG;
     if (!(eps >= 0.f) || !std::isfinite(eps)) return NRC_ERR_INVALID_ARG;
-    if (kernel_size != 3 || stride != 1 || padding != 1 || dilation != 1)
+    const long long T_out_ll = conv1d_out_len(T, kernel_size, stride, padding, dilation);
+    if (T_out_ll <= 0) return NRC_ERR_INVALID_ARG;        // the kernel does not fit the input
+    if (kernel_size > kMaxConvTaps) return NRC_ERR_UNSUPPORTED;
+    if (!conv_positions_fit(T, kernel_size, stride, padding, dilation, T_out_ll))
         return NRC_ERR_UNSUPPORTED;
+    const int T_out = (int)T_out_ll;
     const int cpg = C_out / num_groups;
     if (C_out > 256 && 256 % cpg != 0) return NRC_ERR_UNSUPPORTED;
-    if (ranges_overlap(x, (size_t)N * C_in * T * 4, out, (size_t)N * C_out * T * 4))
+    if (ranges_overlap(x, (size_t)N * C_in * T * 4, out, (size_t)N * C_out * T_out * 4))
         return NRC_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return NRC_ERR_ALIGNMENT;
-    ConvPlan pl = plan_conv(N, C_in, C_out, T, 2, false);
-    if (workspace_bytes < nrc_conv1d_groupnorm_workspace_size(N, C_in, C_out, T, num_groups))
+    ConvPlan pl = plan_conv(N, C_in, C_out, T_out, 2, false, 0, 0, kernel_size);
+    if (workspace_bytes < nrc_conv1d_groupnorm_workspace_size(N, C_in, C_out, T, kernel_size,
+                                                              stride, padding, dilation,
+                                                              num_groups))
         return NRC_ERR_WORKSPACE;
     if ((long long)N * pl.n_tt * pl.n_ot >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
 
@@ -1460,19 +1519,21 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     p.x = x;
     p.out = out;
     // One wave (every tile on its own CTA, all resident): the GroupNorm is
-    // finished inside the GEMM kernel behind a grid-wide barrier.
+    // finished inside the GEMM kernel behind a grid-wide barrier.  Stride 1
+    // with 16-byte aligned rows stages x by TMA boxes; otherwise the prologue
+    // warps load x directly (either kernel also runs the one-wave path).
     p.fused = (pl.g.num_tiles <= device_sm_count() && device_coop_launch()) ? 1 : 0;
-    bool staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
-    if (p.fused && !staged) {           // the one-wave kernel is the staged one
-        p.fused = 0;
-        staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
-    }
+    bool staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T_out, false, T, stride,
+                                          kernel_size);
     p.N = N;
     p.Cin = C_in;
     p.Cout = C_out;
-    p.L = T;
-    p.pad = 1;
-    p.dil = 1;
+    p.L = T_out;
+    p.Lin = T;
+    p.pad = padding;
+    p.dil = dilation;
+    p.stride = stride;
+    p.ksz = kernel_size;
     p.n_tt = pl.n_tt;
     p.n_ot = pl.n_ot;
     p.n_chunks = pl.n_chunks;
@@ -1498,24 +1559,28 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
         p1.gn_beta = gn_beta;
         p1.gn_eps = eps;
         p1.status = device_status_ptr();
-        p1.timeout_ns = wait_timeout_ns();
+        p1.timeout_ns = grid_barrier_timeout_ns();
         if (p1.status == nullptr) return NRC_ERR_CUDA;
         if (cudaMemsetAsync(p1.grid_counter, 0, 2 * sizeof(uint32_t), st) != cudaSuccess)
             return NRC_ERR_CUDA;
         g1.coop = true;
-        const nrc_status s1 = launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true, true>, 2>(
-            "conv_gn_gemm", p1, g1, st);
+        const nrc_status s1 =
+            staged ? launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, true, true>, 2>(
+                         "conv_gn_gemm", p1, g1, st)
+                   : launch_gemm<ConvProblem<float, ConvEpi::kGroupStats, false, true>, 2>(
+                         "conv_gn_gemm", p1, g1, st);
         if (s1 != NRC_ERR_UNSUPPORTED) return s1;
         // refused (the CTAs cannot all be resident now): the two-kernel path,
         // planned without the fused epilogue's shared memory
         p.fused = 0;
-        staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T, false);
+        staged = plan_conv_staged<float>(p, pl, N, C_in, C_out, T_out, false, T, stride,
+                                         kernel_size);
     }
     {
         const size_t units = pl.wpack_bytes / 16 / 2;
         TraceScope ts("pack_conv_weight", st);
         pack_conv_weight_kernel<float, 2><<<elementwise_grid(units), 256, 0, st>>>(
-            conv_weight, ws, C_out, C_in, pl.g.BN, pl.n_ot, pl.n_chunks);
+            conv_weight, ws, C_out, C_in, pl.g.BN, pl.n_ot, pl.n_chunks, kernel_size);
         if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
         pl.g.b_after_prev = true;      // the GEMM launched behind the repack
     }
@@ -1528,7 +1593,7 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     {
         TraceScope ts("groupnorm_finalize_normalize", st);
         groupnorm_finalize_normalize_kernel<<<N * num_groups, 256, 0, st>>>(
-            out, p.partials, pl.n_tt, C_out, T, num_groups, gn_gamma, gn_beta, eps);
+            out, p.partials, pl.n_tt, C_out, T_out, num_groups, gn_gamma, gn_beta, eps);
     }
     return cuda_status(cudaGetLastError());
 }

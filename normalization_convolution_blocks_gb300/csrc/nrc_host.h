@@ -14,6 +14,9 @@ namespace nrc {
 int* device_status_ptr();
 // Current limit of every device-side wait (ns).
 unsigned long long wait_timeout_ns();
+// Current limit of the one-wave GroupNorm kernel's grid-wide barrier (ns): its
+// own setting if one was made, else wait_timeout_ns().
+unsigned long long grid_barrier_timeout_ns();
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 // Whether the current device supports cooperative launches (cached per device).

@@ -15,7 +15,8 @@ identity:
   ~U(+-1/sqrt(3C)).  Draw order: x, rm, rv, gamma, beta, W, bias.  The
   training-mode workload draws the same tensors (rm, rv are then the running
   buffers' starting values; BatchNorm momentum 0.1).
-* conv + GroupNorm: x ~N(0,1); W ~U(+-1/sqrt(3*C_in)); gamma ~U(0.5,1.5);
+* conv + GroupNorm: x ~N(0,1); W (C_out, C_in, k) ~U(+-1/sqrt(k*C_in)), k = 3
+  unless another kernel size is asked for; gamma ~U(0.5,1.5);
   beta ~U(-0.5,0.5).  Draw order: x, W, gamma, beta.
 * Linear + BN + bias + divide + Swish: x ~N(0,1); W, b_lin ~U(+-1/sqrt(IN));
   gamma = 1, beta = 0 (module defaults) unless ``random_affine``, then
@@ -86,11 +87,11 @@ class ConvGNInputs:
     bias: torch.Tensor | None = None
 
 
-def conv_groupnorm_inputs(N, Cin, Cout, T, num_groups, seed=0, eps=1e-5):
+def conv_groupnorm_inputs(N, Cin, Cout, T, num_groups, seed=0, eps=1e-5, kernel_size=3):
     g = torch.Generator("cpu").manual_seed(seed)
     x = _normal(g, (N, Cin, T))
-    bound = 1.0 / math.sqrt(3 * Cin)
-    w = _uniform(g, (Cout, Cin, 3), -bound, bound)
+    bound = 1.0 / math.sqrt(kernel_size * Cin)
+    w = _uniform(g, (Cout, Cin, kernel_size), -bound, bound)
     gamma = _uniform(g, (Cout,), 0.5, 1.5)
     beta = _uniform(g, (Cout,), -0.5, 0.5)
     return ConvGNInputs(x, w, gamma, beta, int(num_groups), eps)

@@ -175,6 +175,11 @@ def prenorm_block_train(x, running_mean, running_var, gamma, beta, eps, momentum
     return out, rm, rv, bm, bv
 
 
+def conv1d_out_len(T, K, stride=1, padding=1, dilation=1):
+    """Conv1d output length (<= 0 when the kernel does not fit the padded input)."""
+    return int(_load().oracle_conv1d_out_len(T, K, stride, padding, dilation))
+
+
 def conv_groupnorm(x, w, bias, num_groups, gamma, beta, eps, stride=1, padding=1,
                    dilation=1, nthreads=0):
     """Conv1d (x (N, Cin, T), w (Cout, Cin, K)) followed by GroupNorm.  Returns

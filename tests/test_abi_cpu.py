@@ -55,6 +55,7 @@ def test_workspace_queries(lib):
     assert api.prenorm_dilconv_residual_workspace_size(256, dtype=None) == 12 * 256 * 128 + 256
     assert lib.nrc_prenorm_dilconv_residual_workspace_size(0, 0) == 0
     assert api.conv1d_groupnorm_workspace_size(16, 128, 256, 1024, 32) > 0
+    assert api.conv1d_output_length(1024, 3, 1, 1, 1) == 1024
     assert api.linear_bn_swish_workspace_size(1024, 8192, 8192) > 2 * 1024 * 8192 * 2
 
 
@@ -144,12 +145,45 @@ def _gn(lib, **kw):
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(x=None), 1), (dict(G=0), 1), (dict(G=3), 1), (dict(g=None), 1),
-    (dict(k=5), 2), (dict(s=2), 2), (dict(p=0), 2), (dict(d=2), 2),
+    (dict(k=0), 1), (dict(s=0), 1), (dict(p=-1), 1), (dict(d=0), 1),
+    (dict(T=4, k=5, p=0), 1),                                  # the kernel does not fit
+    (dict(T=10, k=3, p=0, d=5), 1),                            # nor with dilation
+    (dict(k=65, p=40), 2),                                     # more than 64 taps
+    (dict(p=1 << 29), 2),                                      # positions overflow 32 bits
     (dict(Cout=768, G=64), 2),                                 # 12 channels/group, 768 > 256
     (dict(wsb=8), 4), (dict(ws=ctypes.c_void_p(0x30000008)), 3),
+    (dict(k=5, p=2, wsb="k3"), 4),                             # sized for 3 taps, not 5
+    (dict(s=1, p=20, wsb="p1"), 4),                            # sized for T_out = T, not T+38
 ])
 def test_groupnorm_validation(lib, kw, expect):
+    if kw.get("wsb") == "k3":
+        kw["wsb"] = lib.nrc_conv1d_groupnorm_workspace_size(2, 8, 16, 32, 3, 1, 1, 1, 4)
+    elif kw.get("wsb") == "p1":
+        kw["wsb"] = lib.nrc_conv1d_groupnorm_workspace_size(2, 8, 16, 32, 3, 1, 1, 1, 4)
+        # a workspace for T=32 rows is one 128-row tile: T_out=70 still fits one
+        # tile, so make the conv reach a second tile
+        kw["T"] = 120
     assert _gn(lib, **kw) == expect
+
+
+@pytest.mark.parametrize("T,k,s,p,d", [
+    (1024, 3, 1, 1, 1), (1024, 3, 2, 1, 1), (1000, 5, 3, 4, 2), (10, 3, 1, 0, 5),
+    (7, 1, 1, 0, 1), (100, 4, 1, 5, 1), (50, 7, 2, 0, 3), (1, 1, 1, 0, 1), (5, 9, 1, 2, 1),
+])
+def test_conv_output_length_matches_oracle(lib, T, k, s, p, d):
+    import oracle
+    want = oracle.conv1d_out_len(T, k, s, p, d)
+    assert lib.nrc_conv1d_output_length(T, k, s, p, d) == max(want, 0)
+
+
+def test_groupnorm_workspace_grows_with_taps_and_output_length(lib):
+    f = lib.nrc_conv1d_groupnorm_workspace_size
+    base = f(16, 128, 256, 1024, 3, 1, 1, 1, 32)
+    assert f(16, 128, 256, 1024, 5, 1, 2, 1, 32) > base        # two more taps of weights
+    assert f(16, 128, 256, 1024, 3, 2, 1, 1, 32) < base        # half the output rows
+    assert f(16, 128, 256, 1024, 3, 1, 200, 1, 32) > base      # T_out = T + 398
+    assert f(16, 128, 256, 4, 9, 1, 0, 1, 32) == 0             # kernel longer than input
+    assert f(16, 128, 256, 1024, 0, 1, 1, 1, 32) == 0
 
 
 def _lin(lib, **kw):

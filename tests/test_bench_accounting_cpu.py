@@ -1,6 +1,6 @@
 """bench.py's workload accounting on CPU: FLOP and byte counts in closed form,
 the training-mode workload charged like the eval block, the oracle samplers'
-units, and the recorded DRAM counters pointing at committed profiles."""
+units, and the recorded DRAM counters."""
 import os
 
 import pytest
@@ -51,10 +51,9 @@ def test_block_sampler_counts_flops_per_row(name):
     assert run(2) == 2 * (2 * 32 * 3 * 512)       # two rows of C*3 MACs per position
 
 
-def test_recorded_dram_counters_name_committed_profiles():
+def test_recorded_dram_counters_are_well_formed():
     for name, rec in bench.NCU_TRAFFIC.items():
         assert name in syn.WORKLOADS
-        assert os.path.exists(os.path.join(ROOT, rec["profile"])), rec["profile"]
         assert rec["bytes"] > 0 and len(rec["src_hash"]) == 16
 
 
@@ -74,7 +73,7 @@ def test_json_line_assembly_with_a_stubbed_gpu_arm(monkeypatch, capsys):
                 roofline=dict(bound="tensor", achieved=430.0, peak=963.2, unit="TFLOP/s",
                               frac=0.446, traffic=None),
                 kernels={}, clocks=dict(sm_mhz=2070.0, sm_max_mhz=2070.0, reasons=[]),
-                info=info, step_ms_p10=0.119, step_ms_p90=0.121,
+                info=info, step_ms_p10=0.119, step_ms_p90=0.121, step_ms_median=0.12,
                 e2e=dict(value=50.0, unit="TFLOP/s", h2d_bytes_per_step=1,
                          d2h_bytes_per_step=1))
     monkeypatch.setattr(bench, "gpu_arm", lambda args, world, rank, local: fake)
@@ -85,7 +84,8 @@ def test_json_line_assembly_with_a_stubbed_gpu_arm(monkeypatch, capsys):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
-                "roofline", "e2e", "gpu_launches", "clocks", "bandwidth"):
+                "roofline", "e2e", "gpu_launches", "clocks", "bandwidth",
+                "ms_per_call_median"):
         assert key in line, key
     assert line["n_gpus"] == 1 and line["value"] == 430.0 and line["warmup"] >= 3
     assert line["config"]["workload"] == "prenorm_block_f32"

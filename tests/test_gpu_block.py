@@ -5,20 +5,23 @@ import torch
 
 import oracle
 from normalization_convolution_blocks_gb300 import synthetic as syn
-from gpu_util import assert_bf16, assert_f32, need_gpu, to
+from gpu_util import Guarded, assert_bf16, assert_f32, need_gpu, to
 
 pytestmark = pytest.mark.gpu
 
 
 def _gpu(dev, inp, **kw):
+    """One call into a guarded output buffer; the guards are checked after it."""
     from normalization_convolution_blocks_gb300 import api
     w = kw.get("w", inp.weight)
     b = kw.get("bias", inp.bias)
+    g = Guarded(tuple(inp.x.shape), inp.x.dtype, dev)
     out = api.prenorm_dilconv_residual(to(dev, inp.x), to(dev, inp.running_mean),
                                        to(dev, inp.running_var), to(dev, inp.gamma),
                                        to(dev, inp.beta), inp.eps, to(dev, w), to(dev, b),
-                                       inp.dilation)
+                                       inp.dilation, out=g.view)
     assert api.query_status() == api.NRC_OK
+    g.check(f"block {tuple(inp.x.shape)} d{inp.dilation}")
     return out.double().cpu().numpy()
 
 
@@ -116,30 +119,34 @@ def test_bf16_shapes(N, C, L, d):
     assert_bf16(_gpu(dev, inp), _oracle(inp), f"bf16 N{N} C{C} L{L} d{d}")
 
 
-def test_full_workload_fp32_sampled_rows():
+def test_full_workload_fp32_every_element():
     """The full-size workload (N=32 C=256 L=4096 d=128) in the bench's launch
-    configuration, compared on 48 sampled output rows (all L positions)."""
+    configuration, compared with the oracle on every output element, and
+    also per tile: each 128-row x 256-channel tile of every sample must meet
+    the bar on its own, so an error confined to a few tiles cannot hide in
+    the global norm."""
     dev = need_gpu()
     inp = syn.WORKLOADS["prenorm_block_f32"].make(seed=0)
     got = _gpu(dev, inp)
-    rng = np.random.default_rng(0)
-    rn = np.concatenate([[0, 31, 31], rng.integers(0, 32, 45)])
-    ro = np.concatenate([[0, 255, 128], rng.integers(0, 256, 45)])
-    ref = oracle.prenorm_block_rows(inp.x, inp.running_mean, inp.running_var, inp.gamma,
-                                    inp.beta, inp.eps, inp.weight, inp.bias, inp.dilation, rn, ro)
-    assert_f32(got[rn, ro], ref, "full workload rows")
+    ref = oracle.prenorm_block(inp.x, inp.running_mean, inp.running_var, inp.gamma, inp.beta,
+                               inp.eps, inp.weight, inp.bias, inp.dilation)
+    assert_f32(got, ref, "full workload, every element")
+    N, C, L = got.shape
+    for n in range(N):
+        for t0 in range(0, L, 128):
+            assert_f32(got[n, :, t0:t0 + 128], ref[n, :, t0:t0 + 128], f"tile n{n} t{t0}")
 
 
 @pytest.mark.parametrize("C,d", [(C, d) for C in (256, 512) for d in (1, 8, 128, 512)])
-def test_full_bf16_workload_sampled_rows(C, d):
+def test_full_bf16_workload_every_element(C, d):
     dev = need_gpu()
     inp = syn.WORKLOADS[f"prenorm_block_bf16_C{C}_d{d}"].make(seed=0)
     got = _gpu(dev, inp)
-    rng = np.random.default_rng(1)
-    rn, ro = rng.integers(0, 8, 24), rng.integers(0, C, 24)
-    ref = oracle.prenorm_block_rows(inp.x, inp.running_mean, inp.running_var, inp.gamma,
-                                    inp.beta, inp.eps, inp.weight, inp.bias, inp.dilation, rn, ro)
-    assert_bf16(got[rn, ro], ref, f"bf16 full C{C} d{d} rows")
+    ref = oracle.prenorm_block(inp.x, inp.running_mean, inp.running_var, inp.gamma, inp.beta,
+                               inp.eps, inp.weight, inp.bias, inp.dilation)
+    assert_bf16(got, ref, f"bf16 full C{C} d{d}, every element")
+    for n in range(got.shape[0]):
+        assert_bf16(got[n], ref[n], f"bf16 full C{C} d{d}, sample {n}")
 
 
 def test_repeat_calls_identical():
@@ -152,10 +159,12 @@ def test_repeat_calls_identical():
 def _host_call(inp, chunk_n, pinned=True):
     from normalization_convolution_blocks_gb300 import api
     x = inp.x.pin_memory() if pinned else inp.x
+    g = Guarded(tuple(inp.x.shape), inp.x.dtype, pinned=True)
     out = api.prenorm_dilconv_residual(x, inp.running_mean, inp.running_var, inp.gamma,
                                        inp.beta, inp.eps, inp.weight, inp.bias, inp.dilation,
-                                       chunk_n=chunk_n)
+                                       chunk_n=chunk_n, out=g.view)
     assert not out.is_cuda and api.query_status() == api.NRC_OK
+    g.check(f"host entry chunk {chunk_n}")
     return out.double().numpy()
 
 
@@ -192,19 +201,19 @@ def test_bf16_views_at_odd_offsets(which):
     inp = syn.prenorm_block_inputs(2, 64, 256, 4, seed=17, dtype=torch.bfloat16)
     n = inp.x.numel()
     x = to(dev, inp.x)
-    out = None
+    g = Guarded(tuple(inp.x.shape), torch.bfloat16, dev, offset=1 if which == "out" else 0)
+    out = g.view
     if which == "x":
         xb = torch.empty(n + 1, dtype=torch.bfloat16, device=dev)
         xb[1:].copy_(x.reshape(-1))
         x = xb[1:].view(inp.x.shape)
-    else:
-        out = torch.empty(n + 1, dtype=torch.bfloat16, device=dev)[1:].view(inp.x.shape)
     assert (x if which == "x" else out).data_ptr() % 8 == 2
     got = api.prenorm_dilconv_residual(x, to(dev, inp.running_mean), to(dev, inp.running_var),
                                        to(dev, inp.gamma), to(dev, inp.beta), inp.eps,
                                        to(dev, inp.weight), to(dev, inp.bias), inp.dilation,
                                        out=out)
     assert api.query_status() == api.NRC_OK
+    g.check(f"bf16 {which} at +2 bytes")
     assert_bf16(got.double().cpu().numpy(), _oracle(inp), f"bf16 {which} at +2 bytes")
 
 
@@ -229,13 +238,14 @@ def test_back_to_back_calls_with_alternating_weights(N, C, L, d):
     for w in ws:
         ref.append(api.prenorm_dilconv_residual(*args, inp.eps, w, bias, inp.dilation).clone())
         torch.cuda.synchronize()
-    outs = [torch.empty_like(args[0]) for _ in range(6)]
+    guards = [Guarded(tuple(args[0].shape), args[0].dtype, dev) for _ in range(6)]
     workspace = torch.empty(api.prenorm_dilconv_residual_workspace_size(C), dtype=torch.uint8,
                             device=dev)
-    for i, o in enumerate(outs):           # one stream, shared workspace, no syncs
-        api.prenorm_dilconv_residual(*args, inp.eps, ws[i % 2], bias, inp.dilation, out=o,
+    for i, g in enumerate(guards):         # one stream, shared workspace, no syncs
+        api.prenorm_dilconv_residual(*args, inp.eps, ws[i % 2], bias, inp.dilation, out=g.view,
                                      workspace=workspace)
     torch.cuda.synchronize()
     assert api.query_status() == api.NRC_OK
-    for i, o in enumerate(outs):
-        assert torch.equal(o, ref[i % 2]), f"call {i}"
+    for i, g in enumerate(guards):
+        g.check(f"call {i}")
+        assert torch.equal(g.view, ref[i % 2]), f"call {i}"

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from normalization_convolution_blocks_gb300 import synthetic as syn
-from gpu_util import RUNNING_STAT_ABS, assert_bf16, assert_f32, need_gpu, to
+from gpu_util import RUNNING_STAT_ABS, Guarded, assert_bf16, assert_f32, need_gpu, to
 
 pytestmark = pytest.mark.gpu
 
@@ -20,11 +20,13 @@ def _gpu(dev, inp, momentum=0.1, x=None, buffers=True):
     rv = to(dev, inp.running_var).clone() if buffers else None
     nbt = torch.zeros(1, dtype=torch.int64, device=dev) if buffers else None
     xd = to(dev, inp.x) if x is None else x
+    g = Guarded(tuple(xd.shape), xd.dtype, dev)
     out = api.prenorm_dilconv_residual_train(xd, rm, rv, to(dev, inp.gamma), to(dev, inp.beta),
                                              inp.eps, momentum, to(dev, inp.weight),
                                              to(dev, inp.bias), inp.dilation,
-                                             num_batches_tracked=nbt)
+                                             num_batches_tracked=nbt, out=g.view)
     assert api.query_status() == api.NRC_OK
+    g.check(f"training-mode block {tuple(xd.shape)}")
     cpu = (lambda t: None if t is None else t.double().cpu().numpy())
     return cpu(out), cpu(rm), cpu(rv), (None if nbt is None else int(nbt.item()))
 

@@ -5,23 +5,30 @@ import torch
 
 import oracle
 from normalization_convolution_blocks_gb300 import synthetic as syn
-from gpu_util import assert_f32, need_gpu, to
+from gpu_util import Guarded, assert_f32, need_gpu, to
 
 pytestmark = pytest.mark.gpu
 
 
-def _gpu(dev, g, G, bias=None, affine=True):
+def _gpu(dev, g, G, bias=None, affine=True, stride=1, padding=1, dilation=1):
     from normalization_convolution_blocks_gb300 import api
+    N, _, T = g.x.shape
+    Cout, _, k = g.weight.shape
+    T_out = api.conv1d_output_length(T, k, stride, padding, dilation)
+    gd = Guarded((N, Cout, T_out), torch.float32, dev)
     out = api.conv1d_groupnorm(to(dev, g.x), to(dev, g.weight), to(dev, bias), G,
                                to(dev, g.gamma) if affine else None,
-                               to(dev, g.beta) if affine else None, g.eps)
+                               to(dev, g.beta) if affine else None, g.eps, stride=stride,
+                               padding=padding, dilation=dilation, out=gd.view)
     assert api.query_status() == api.NRC_OK
+    gd.check(f"conv+GN N{N} {Cout} T_out{T_out}")
     return out.double().cpu().numpy()
 
 
-def _ref(g, G, bias=None, affine=True):
+def _ref(g, G, bias=None, affine=True, stride=1, padding=1, dilation=1):
     return oracle.conv_groupnorm(g.x, g.weight, bias, G, g.gamma if affine else None,
-                                 g.beta if affine else None, g.eps)
+                                 g.beta if affine else None, g.eps, stride=stride,
+                                 padding=padding, dilation=dilation)
 
 
 def test_full_workload():
@@ -86,3 +93,52 @@ def test_full_workload_group_stats():
     for r, (n, gg) in enumerate([(0, 0), (15, 31)]):
         s2 = mv[r, 1]
         assert abs(per[n, gg].var() - s2 / (s2 + g.eps)) < 1e-5
+
+
+# General conv parameters (the module's kernel_size, stride, padding and
+# dilation).  Stride 1 stages x by TMA boxes; stride > 1 loads it directly.
+# Each case runs on one wave of resident CTAs (the fused kernel) and on more
+# tiles than SMs (GEMM + finalize kernel), with the affine on and off.
+GENERAL = [
+    # (k, stride, padding, dilation)
+    (3, 2, 1, 1),
+    (3, 1, 2, 2),
+    (5, 1, 2, 1),
+    (5, 3, 4, 2),
+    (1, 1, 0, 1),         # pointwise
+    (7, 2, 0, 3),         # no padding: the output is shorter than the input
+    (4, 1, 5, 1),         # even kernel, padding larger than half the span (T_out > T)
+]
+
+
+@pytest.mark.parametrize("k,s,pad,d", GENERAL)
+@pytest.mark.parametrize("affine", [True, False])
+@pytest.mark.parametrize("wave", ["one", "multi"])
+def test_general_conv_parameters(k, s, pad, d, affine, wave):
+    dev = need_gpu()
+    from normalization_convolution_blocks_gb300 import api
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if wave == "one":
+        N, Cin, Cout, T, G = 2, 40, 96, 700, 12       # 8 ch/group, ragged Cin
+    else:
+        N, Cin, Cout, T, G = 3, 24, 64, 8000 * s, 8   # > SMs tiles
+    T_out = api.conv1d_output_length(T, k, s, pad, d)
+    assert T_out == oracle.conv1d_out_len(T, k, s, pad, d) > 0
+    n_tiles = N * -(-T_out // 128) * -(-Cout // 256)
+    assert (n_tiles <= sms) == (wave == "one"), n_tiles
+    g = syn.conv_groupnorm_inputs(N, Cin, Cout, T, G, seed=k * 100 + s * 10 + pad + d,
+                                  kernel_size=k)
+    kw = dict(affine=affine, stride=s, padding=pad, dilation=d)
+    got = _gpu(dev, g, G, **kw)
+    assert got.shape == (N, Cout, T_out)
+    assert_f32(got, _ref(g, G, **kw), f"k{k} s{s} p{pad} d{d} affine={affine} {wave} wave")
+
+
+def test_general_conv_with_bias_and_unaligned_rows():
+    """T not a multiple of 4 (rows not 16-byte aligned: no TMA boxes) with a
+    dilated, padded kernel and a conv bias."""
+    dev = need_gpu()
+    g = syn.conv_groupnorm_inputs(2, 33, 48, 301, 6, seed=77, kernel_size=5)
+    bias = torch.linspace(-0.5, 0.5, 48)
+    kw = dict(bias=bias, stride=1, padding=3, dilation=2)
+    assert_f32(_gpu(dev, g, 6, **kw), _ref(g, 6, **kw), "k5 d2 p3 T301 with bias")
