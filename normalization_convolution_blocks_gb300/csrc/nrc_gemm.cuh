@@ -304,6 +304,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 return true;
             };
+            // Descriptor of B ring slot 0; slot s, row c0 lies (s*stage + c0*128)
+            // bytes further, i.e. that >> 4 more in the start-address field
+            // (the ring lies far below the field's 256 KB limit).
+            const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(smem));
+            const uint32_t a_ring = tmem_base + kTmemARing;
             // MMAs of the stage i past the cursors into columns [c0, c0 + n) (B
             // rows c0 ..); `first` starts that column range afresh.
             auto mma_stage = [&](int i, int c0, uint32_t idesc, bool first) {
@@ -311,22 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t ph;
                 a_at(i, s_a, ph);
                 b_at(i, s_b, ph);
-                const uint32_t a_col = tmem_base + kTmemARing + (uint32_t)(s_a * 32 * NP);
-                const uint32_t b_hi =
-                    smem_u32(smem + (size_t)s_b * cfg.b_stage_bytes) + (uint32_t)c0 * 128u;
-                const uint32_t d = tmem_base + (uint32_t)c0;
-#pragma unroll
-                for (int kk = 0; kk < kBK / kUMMA_K; ++kk) {
-                    const uint32_t a_k = a_col + (uint32_t)(kk * kUMMA_K / 2);
-                    const uint64_t bd = sw128_kmajor_desc(b_hi + (uint32_t)kk * (kUMMA_K * 2));
-                    mma_bf16_ts(d, a_k, bd, idesc, (first && kk == 0) ? 0u : 1u);
-                    if constexpr (NP == 2) {
-                        const uint64_t bd_lo = sw128_kmajor_desc(
-                            b_hi + (uint32_t)BN * 128u + (uint32_t)kk * (kUMMA_K * 2));
-                        mma_bf16_ts(d, a_k + 32u, bd, idesc, 1u);   // lo * hi
-                        mma_bf16_ts(d, a_k, bd_lo, idesc, 1u);      // hi * lo
-                    }
-                }
+                const uint64_t bd =
+                    bdesc0 + (uint64_t)(((uint32_t)s_b * cfg.b_stage_bytes + (uint32_t)c0 * 128u) >> 4);
+                mma_stage_bf16<NP>(tmem_base + (uint32_t)c0, a_ring + (uint32_t)(s_a * 32 * NP), bd,
+                                   bd + (uint64_t)(((uint32_t)BN * 128u) >> 4), idesc,
+                                   first ? 0u : 1u);
             };
             // Frees the stage at the cursors once its MMAs finish; advances.
             auto retire = [&]() {

@@ -218,6 +218,53 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// One K=64 stage of MMAs in a single asm block: A from TMEM at column a (K
+// packed two bf16 per column: kk-th K=16 slice at a + 8*kk), B through the
+// 128B-swizzled K-major descriptor bd (kk-th slice at start address + 32*kk
+// bytes, i.e. descriptor + 2*kk).  kParts = 1: bf16 storage, four MMAs.
+// kParts = 2: fp32 storage split v = hi + lo, twelve MMAs in the order
+// hi*hi, lo*hi, hi*lo per slice; the A lo part sits 32 columns after hi, the
+// B lo image at descriptor bd_lo.  `acc` = 0 starts the accumulator afresh
+// with the first MMA.  One thread issues; keeping the per-MMA work to
+// immediate adds lets it issue as fast as the tensor pipe runs.
+template <int kParts>
+__device__ __forceinline__ void mma_stage_bf16(uint32_t d, uint32_t a, uint64_t bd,
+                                               uint64_t bd_lo, uint32_t idesc, uint32_t acc) {
+    if constexpr (kParts == 1) {
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "setp.eq.b32 q, %4, %4;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], %5, %3, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], %6, %3, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], %7, %3, q;\n\t}"
+            ::"r"(d), "r"(a), "l"(bd), "r"(idesc), "r"(acc), "l"(bd + 2), "l"(bd + 4),
+            "l"(bd + 6)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.b32 p, %5, 0;\n\t"
+            "setp.eq.b32 q, %5, %5;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], %2, %4, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %4, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], %6, %4, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], %6, %4, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], %7, %4, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], %8, %4, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], %8, %4, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], %9, %4, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], %10, %4, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], %10, %4, q;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], %11, %4, q;\n\t}"
+            ::"r"(d), "r"(a), "l"(bd), "l"(bd_lo), "r"(idesc), "r"(acc), "l"(bd + 2),
+            "l"(bd_lo + 2), "l"(bd + 4), "l"(bd_lo + 4), "l"(bd + 6), "l"(bd_lo + 6)
+            : "memory");
+    }
+}
+
 // 32 lanes x 16 consecutive 32-bit columns from registers (each thread its
 // own lane), completed (wait::st) before returning.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
