@@ -236,14 +236,16 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[COLS]) {
 template <int CPG>
 __device__ __forceinline__ void gn_tile_stats(const float* bias_s, uint32_t taddr, int ovalid,
                                               int ng, float tw, float inv_nvr, float wcount,
-                                              int quarter, int lane, float4* s_part) {
+                                              int quarter, int lane, float4* s_part,
+                                              bool has_bias) {
     constexpr int COLS = CPG == 1 ? 16 : (CPG <= 4 ? 32 : 64);
     constexpr int NB = COLS / CPG;                      // groups per batch
     for (int cb = 0; cb < ovalid; cb += COLS) {         // COLS divides 256: no batch
         float v[COLS];                                  // crosses the accumulator
         tmem_ld_cols<COLS>(taddr + (uint32_t)cb, v);
 #pragma unroll
-        for (int i = 0; i < COLS; ++i) v[i] = cb + i < ovalid ? v[i] + bias_s[cb + i] : 0.f;
+        for (int i = 0; i < COLS; ++i)
+            v[i] = cb + i < ovalid ? (has_bias ? v[i] + bias_s[cb + i] : v[i]) : 0.f;
         float m[NB], q[NB];
 #pragma unroll
         for (int k = 0; k < NB; ++k) {
@@ -315,10 +317,12 @@ struct ConvProblem {
 
     static __device__ void setup(const Params& p, uint8_t* extra, int tid, int nthr) {
         if constexpr (ONE_WAVE) {
-            // this CTA's share of the weight image, published to the copy engine
+            // this CTA's share of the weight image, published to the copy engine.
+            // Unit u goes to CTA u % gridDim.x, so every CTA packs about the
+            // same number of units: the B producers wait for the slowest CTA.
             constexpr int NP = sizeof(T) == 4 ? 2 : 1;
             const size_t units = (size_t)p.n_ot * p.n_kiters * p.BN * 8;
-            for (size_t idx = (size_t)blockIdx.x * nthr + tid; idx < units;
+            for (size_t idx = (size_t)tid * gridDim.x + blockIdx.x; idx < units;
                  idx += (size_t)gridDim.x * nthr)
                 pack_conv_chunk<T, NP>(static_cast<const T*>(p.w_raw), p.wpack_out, p.Cout,
                                        p.Cin, p.BN, p.n_chunks, p.ksz, idx);
@@ -332,17 +336,6 @@ struct ConvProblem {
         // (32 zero floats past the last tile, so vector reads never leave the region)
         for (int o = tid; o < p.n_ot * p.BN + 32; o += nthr)
             ex[p.bias_off + o] = (bias && o < p.Cout) ? load_f<T>(bias + o) : 0.f;
-        if constexpr (ONE_WAVE && EPI == ConvEpi::kGroupStats) {
-            // one tile per CTA: its channels' gamma and beta, staged while the
-            // mainloop runs (the epilogue turns them into scale and shift)
-            const int obase = conv_tile(p, (int)blockIdx.x).ot * p.BN;
-            float* s_a = reinterpret_cast<float*>(extra + p.stage_off + kGnMaxGroups * 4 * 16);
-            for (int c = tid; c < 256; c += nthr) {
-                const int o = obase + c;
-                s_a[c] = (p.gn_gamma && o < p.Cout) ? p.gn_gamma[o] : 1.f;
-                s_a[256 + c] = (p.gn_beta && o < p.Cout) ? p.gn_beta[o] : 0.f;
-            }
-        }
         if (p.rm == nullptr) return;
         // BN fold: z = max(0, x*scale + shift), scale = gamma/sqrt(rv+eps),
         // shift = beta - rm*scale.  Channels past Cin get 0.
@@ -629,6 +622,19 @@ struct ConvProblem {
             // M2), folded into the group's running triple with Chan's update,
             // and merged across the warp when the group ends.  Every test below
             // is uniform across the warp except t_ok (invalid rows count 0).
+            if constexpr (ONE_WAVE) {
+                // one tile per CTA: its channels' gamma and beta, staged by the
+                // epilogue warps while the mainloop runs (step 3 of gn_fused
+                // turns them into scale and shift, behind its first barrier)
+                float* s_a =
+                    reinterpret_cast<float*>(const_cast<uint8_t*>(extra) + p.stage_off +
+                                             kGnMaxGroups * 4 * 16);
+                for (int c = quarter * 32 + lane; c < 256; c += 128) {
+                    const int o = obase + c;
+                    s_a[c] = (p.gn_gamma && o < p.Cout) ? p.gn_gamma[o] : 1.f;
+                    s_a[256 + c] = (p.gn_beta && o < p.Cout) ? p.gn_beta[o] : 0.f;
+                }
+            }
             bool acquired = true;
             for (int h = 0; h < halves && acquired; ++h) acquired = acquire(h);
             if constexpr (ONE_WAVE) {
@@ -770,15 +776,16 @@ struct ConvProblem {
         // 1. group statistics of the tile.  Every valid row of a group has the
         //    same count (cpg), so the warp's merge of its rows is two warp sums:
         //    of the row means, then of M2_r + cpg*(mean_r - mean)^2.
+        const bool has_bias = p.bias != nullptr;
         const int nvr = __popc(__ballot_sync(0xffffffffu, t_ok));   // valid rows of the warp
         const float inv_nvr = nvr > 0 ? 1.f / (float)nvr : 0.f;
         const float wcount = (float)(p.cpg * nvr);
         switch (p.cpg) {
-            case 1: gn_tile_stats<1>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part); break;
-            case 2: gn_tile_stats<2>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part); break;
-            case 4: gn_tile_stats<4>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part); break;
-            case 8: gn_tile_stats<8>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part); break;
-            case 16: gn_tile_stats<16>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part); break;
+            case 1: gn_tile_stats<1>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part, has_bias); break;
+            case 2: gn_tile_stats<2>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part, has_bias); break;
+            case 4: gn_tile_stats<4>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part, has_bias); break;
+            case 8: gn_tile_stats<8>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part, has_bias); break;
+            case 16: gn_tile_stats<16>(bias_s, taddr, ovalid, ng, tw, inv_nvr, wcount, quarter, lane, s_part, has_bias); break;
             default: {
                 // groups crossing 16-channel chunks: each row's (count, mean, M2)
                 // over the group's runs, then the warp sums at its last run
@@ -871,7 +878,9 @@ struct ConvProblem {
                 const int cl = gl * p.cpg + i;             // channel within the tile
                 const float a = inv * s_a[cl];
                 s_a[cl] = a;
-                s_sh[cl] = s_sh[cl] - m * a;
+                // out = (y - mean)*a + beta with y = acc + bias: the conv bias
+                // folds into the shift, so step 4 reads the accumulator alone
+                s_sh[cl] = s_sh[cl] - (m - bias_s[cl]) * a;
             }
         }
         named_bar_sync(1, 128);
@@ -887,15 +896,13 @@ struct ConvProblem {
                 if (t_ok) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
-                        store_f<T>(op + (size_t)i * p.L,
-                                   fmaf(v[i] + bias_s[cb + i], s_a[cb + i], s_sh[cb + i]));
+                        store_f<T>(op + (size_t)i * p.L, fmaf(v[i], s_a[cb + i], s_sh[cb + i]));
                 }
             } else {
 #pragma unroll
                 for (int i = 0; i < 64; ++i)
                     if (t_ok && cb + i < ovalid)
-                        store_f<T>(op + (size_t)i * p.L,
-                                   fmaf(v[i] + bias_s[cb + i], s_a[cb + i], s_sh[cb + i]));
+                        store_f<T>(op + (size_t)i * p.L, fmaf(v[i], s_a[cb + i], s_sh[cb + i]));
             }
         }
         return true;
