@@ -68,6 +68,8 @@ struct ConvParams {
     float bn_eps;
     const void* bias;       // (Cout) or NULL
     int bias_off;           // float offset of the staged bias in the extra smem
+    int bn2_off;            // bf16 storage: word offset of the BN scale and shift as packed
+                            // bf16 pairs (channels 2i, 2i+1), n_chunks*32 words each
     int stage_off;          // byte offset of the bf16 epilogue's two chunk buffers (staged bf16)
     const uint8_t* wpack;   // packed weight image
     // in-kernel weight repack (pack_counter != NULL): every CTA packs a share of
@@ -350,6 +352,24 @@ struct ConvProblem {
             sc[c] = sv;
             sh[c] = h;
         }
+        if constexpr (sizeof(T) == 2) {
+            // the same fold as packed bf16 pairs for the producers' bf16x2 math
+            uint32_t* sc2 = reinterpret_cast<uint32_t*>(extra) + p.bn2_off;
+            uint32_t* sh2 = sc2 + p.n_chunks * (kBK / 2);
+            for (int i = tid; i < p.n_chunks * (kBK / 2); i += nthr) {
+                float sv[2] = {0.f, 0.f}, h[2] = {0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int c = 2 * i + e;
+                    if (c < p.Cin) {
+                        sv[e] = p.gamma[c] / sqrtf(p.rv[c] + p.bn_eps);
+                        h[e] = p.beta[c] - p.rm[c] * sv[e];
+                    }
+                }
+                sc2[i] = pack_bf16x2(sv[0], sv[1]);
+                sh2[i] = pack_bf16x2(h[0], h[1]);
+            }
+        }
     }
 
     // K stage -> (tap, 64-channel chunk): taps outermost.
@@ -406,6 +426,14 @@ struct ConvProblem {
         tma_load_3d(dst, &p.xmap, s & ~(kAlign - 1), chunk * kBK, tl.n, bar);
     }
 
+    // bf16 storage with BN (staged): read_a returns the 16 packed bf16 pairs
+    // (channels 2j, 2j+1 in v[j]'s bits) with BN+ReLU applied in bf16x2
+    // arithmetic -- two values per instruction, nothing widened to fp32 -- so
+    // the eight producer warps leave issue slots to the MMA warp.  The fold's
+    // scale and shift are rounded to bf16 for it; z is rounded to bf16 for
+    // the MMA in either case.
+    static constexpr bool kPackedA = STAGED && sizeof(T) == 2 && EPI == ConvEpi::kResidual;
+
     static __device__ __forceinline__ void read_a(const Params& p, const uint8_t* extra,
                                                   const Tile& tl, int kiter, int row, int k0,
                                                   int lane, uint32_t box, float (&v)[32]) {
@@ -413,6 +441,35 @@ struct ConvProblem {
         stage_tap(p, kiter, tap, chunk);
         const int rem = box_row0(p, tl, tap) & (kAlign - 1);
         const uint32_t a = box + (uint32_t)((k0 * kBoxW + row + rem) * (int)sizeof(T));
+        if constexpr (kPackedA) {
+            const int c0 = chunk * kBK + k0;            // even
+            const uint4* sc4 =
+                reinterpret_cast<const uint4*>(reinterpret_cast<const uint32_t*>(extra) +
+                                               p.bn2_off + c0 / 2);
+            const uint4* sh4 = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const uint32_t*>(extra) + p.bn2_off + p.n_chunks * (kBK / 2) +
+                c0 / 2);
+            const __nv_bfloat162 zero2 = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 s4 = sc4[q], h4 = sh4[q];
+                const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
+                const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 4 * q + e;
+                    const uint32_t lo = ld_shared_u16(a + (uint32_t)((2 * j) * kBoxW * 2));
+                    const uint32_t hi = ld_shared_u16(a + (uint32_t)((2 * j + 1) * kBoxW * 2));
+                    const uint32_t xw = lo | (hi << 16);
+                    __nv_bfloat162 z = __hfma2(*reinterpret_cast<const __nv_bfloat162*>(&xw),
+                                               *reinterpret_cast<const __nv_bfloat162*>(&sw[e]),
+                                               *reinterpret_cast<const __nv_bfloat162*>(&hw[e]));
+                    z = __hmax2(z, zero2);
+                    v[j] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&z));
+                }
+            }
+            return;
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const uint32_t ai = a + (uint32_t)(i * kBoxW * (int)sizeof(T));
@@ -1026,7 +1083,8 @@ static ConvPlan plan_conv(int N, int Cin, int Cout, int L, int NP, bool with_bn,
     pl.n_tt = ceil_div(L, kBM);
     const long long tiles = (long long)N * pl.n_tt * pl.n_ot;
     const uint32_t fold_bias = (with_bn ? (uint32_t)(2 * pl.n_chunks * kBK * 4) : 0u) +
-                               (uint32_t)((pl.n_ot * BN + 32) * 4);
+                               (uint32_t)((pl.n_ot * BN + 32) * 4) +
+                               (with_bn && NP == 1 ? (uint32_t)(pl.n_chunks * kBK * 4) : 0u);
     pl.stage_off = (int)((fold_bias + 127u) & ~127u);
     const uint32_t extra = stage_bytes ? (uint32_t)pl.stage_off + stage_bytes : fold_bias;
     pl.g = make_gemm_plan(BN, (int)std::min<long long>(tiles, 1LL << 30), ksz * pl.n_chunks, NP,
@@ -1150,6 +1208,7 @@ nrc_status block_gemm(const void* x, void* out, nrc_dtype dt, int N, int C, int 
     p.bn_eps = bn_eps;
     p.bias = conv_bias;
     p.bias_off = 2 * pl.n_chunks * kBK;
+    p.bn2_off = p.bias_off + pl.n_ot * pl.g.BN + 32;     // after the staged bias
     p.wpack = wpack;
     // w_raw given: repack it.  One wave (pack_counter given) with the staged
     // kernel: inside the GEMM kernel (cooperative launch); otherwise by the

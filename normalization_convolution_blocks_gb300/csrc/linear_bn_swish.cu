@@ -62,6 +62,7 @@ struct LinearProblem {
     using Params = LinearParams;
     using Tile = LinearTile;
     static constexpr bool kStagedA = STAGED;
+    static constexpr bool kPackedA = false;                    // read_a returns fp32 values
     static constexpr uint32_t kBoxBytes = 2u * 128u * 128u;   // two 32-float x 128-row boxes
 
     // Tiles of one feature block are adjacent, so the CTAs reading the same

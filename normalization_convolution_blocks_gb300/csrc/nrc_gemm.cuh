@@ -135,6 +135,9 @@ __device__ __forceinline__ void split_store_a(uint32_t taddr_hi, const float (&v
 //        -> A[row][kiter*64 + k0 .. +32) from the landed slot, transform applied
 //   static __device__ const void* b_src(const Params&, const Tile&, int kiter)
 //        -> packed B image of the stage: NP parts of BN rows x 128 B, swizzled
+//   static constexpr bool kPackedA
+//        -> (NP == 1) read_a returns the 16 bf16 pairs already packed, their bits
+//           in v[0..16), stored to TMEM as they are
 //   template <class Acquire, class Release>
 //   static __device__ bool epilogue(const Params&, const uint8_t* extra, const Tile&,
 //                                   int quarter, int lane, uint32_t taddr, int BN,
@@ -424,9 +427,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
             if (!w_ok) return false;
             tc_fence_after();
-            split_store_a<NP>(tmem_base + lane_off + kTmemARing + (uint32_t)(sa * 32 * NP) +
-                                  (uint32_t)(k0 / 2),
-                              v);
+            const uint32_t ta = tmem_base + lane_off + kTmemARing + (uint32_t)(sa * 32 * NP) +
+                                (uint32_t)(k0 / 2);
+            if constexpr (Prob::kPackedA && NP == 1) {
+                // already packed bf16 pairs (v[0..16) hold their bits)
+                uint32_t h[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) h[e] = __float_as_uint(v[e]);
+                tmem_st16(ta, h);
+            } else {
+                split_store_a<NP>(ta, v);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full(sa));

@@ -399,6 +399,13 @@ __device__ __forceinline__ float ld_shared_bf16(uint32_t addr) {
     return __uint_as_float((uint32_t)u << 16);
 }
 
+// A 16-bit shared-memory value, zero-extended.
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+    unsigned short u;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(u) : "r"(addr) : "memory");
+    return (uint32_t)u;
+}
+
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, unsigned short v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
