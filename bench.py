@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
     "prenorm_block_f32": {"bytes": 135181568 + 86730496, "src_hash": "9017c6bb33005bc7"},
     "linear_bn_swish_f32": {"bytes": 335579136 + 23328512, "src_hash": "1369cf96589d4849"},
     "linear_bn_swish_eval_f32": {"bytes": 335710976 + 23072256, "src_hash": "1369cf96589d4849"},
-    "prenorm_block_train_f32": {"bytes": 221418240, "src_hash": "41640fe1382ffc87"},
+    "prenorm_block_train_f32": {"bytes": 135194368 + 85964800, "src_hash": "9017c6bb33005bc7"},
     "conv1d_groupnorm_f32": {"bytes": 8893184 + 0, "src_hash": "9017c6bb33005bc7"},
     "prenorm_block_bf16_C256_d1": {"bytes": 67609856 + 22716928, "src_hash": "9017c6bb33005bc7"},
     "prenorm_block_bf16_C256_d512": {"bytes": 67602432 + 23153408, "src_hash": "9017c6bb33005bc7"},
