@@ -348,9 +348,12 @@ def make_call(name, dev, host=False):
         nbt = torch.zeros(1, dtype=torch.int64, device=dev)
         B, IN = x.shape
         OUT = w.shape[0]
-        out = None if host else torch.empty((B, OUT), device=dev)
-        ws = None if host else torch.empty(api.linear_bn_swish_workspace_size(B, IN, OUT),
-                                           dtype=torch.uint8, device=dev)
+        # host buffers: the output is pinned and the workspace allocated once
+        out = torch.empty((B, OUT), pin_memory=True) if host else \
+            torch.empty((B, OUT), device=dev)
+        ws_bytes = api.linear_bn_swish_host_workspace_size(B, IN, OUT) if host else \
+            api.linear_bn_swish_workspace_size(B, IN, OUT)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         tensors_in = (x, w, lb, g, b, ab)
 
         training = wl.params.get("training", True)

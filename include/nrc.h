@@ -275,6 +275,45 @@ nrc_status nrc_linear_bn_swish(
     void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Linear + BatchNorm1d + bias + divide + Swish on HOST buffers (end-to-end
+ * path).  The pages have no counterpart: a library convenience.
+ *
+ * Same computation and argument rules as nrc_linear_bn_swish, with x_host
+ * (B, in_f), out_host (B, out_f), lin_weight_host (out_f, in_f),
+ * lin_bias_host / bn_gamma_host / bn_beta_host (out_f, or NULL as there) and
+ * add_bias_host (one value) in HOST memory (pinned for the copies to overlap),
+ * while bn_running_mean / bn_running_var (and num_batches_tracked) stay DEVICE
+ * buffers, updated in place as in the device entry.
+ * Each output feature's batch statistics involve that feature alone, so the
+ * call runs in chunks of chunk_f output features (rounded up to whole 128-
+ * feature tiles; the first and last chunks are smaller): x is copied in and
+ * packed once, then the copy-in of chunk j+1's weight rows, the chain of
+ * chunk j (GEMM, and in training mode the finalize and normalize kernels) and
+ * the copy-out of chunk j-1's columns run at once, on two library-owned
+ * streams (created once per device) and `stream`, ordered by events.  Results
+ * are bitwise those of nrc_linear_bn_swish.
+ * workspace: DEVICE memory, 256-byte aligned, of at least
+ *   nrc_linear_bn_swish_host_workspace_size(B, in_f, out_f, chunk_f) bytes
+ *   (the x image and statistics for one chunk, x, the parameters, two weight
+ *   and two output chunk buffers); 0 from the query: invalid arguments.
+ * Errors: those of nrc_linear_bn_swish, and NRC_ERR_INVALID_ARG for
+ * chunk_f <= 0.
+ * Asynchronous: work already on `stream` comes first; `stream` resumes after
+ * the last copy-out, so synchronising `stream` makes out_host valid.  Calls
+ * from several host threads are serialised inside the library.
+ * ------------------------------------------------------------------------ */
+size_t nrc_linear_bn_swish_host_workspace_size(int B, int in_f, int out_f, int chunk_f);
+
+nrc_status nrc_linear_bn_swish_host(
+    const float *x_host, float *out_host, int B, int in_f, int out_f,
+    const float *lin_weight_host, const float *lin_bias_host,
+    const float *bn_gamma_host, const float *bn_beta_host,
+    float *bn_running_mean, float *bn_running_var, int64_t *num_batches_tracked,
+    float bn_eps, float bn_momentum, int training,
+    const float *add_bias_host, float divide_value, int chunk_f,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Status and fault handling
  * ------------------------------------------------------------------------ */
 /* Synchronises `stream`, then reads and clears the device status word of the

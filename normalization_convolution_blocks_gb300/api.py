@@ -69,6 +69,9 @@ def load() -> ctypes.CDLL:
         "nrc_conv1d_groupnorm": ([p, p, i, i, i, i, i, i, i, i, p, p, i, p, p, f, p, sz, p], i),
         "nrc_linear_bn_swish_workspace_size": ([i, i, i], sz),
         "nrc_linear_bn_swish": ([p, p, i, i, i, p, p, p, p, p, p, p, f, f, i, p, f, p, sz, p], i),
+        "nrc_linear_bn_swish_host_workspace_size": ([i, i, i, i], sz),
+        "nrc_linear_bn_swish_host": ([p, p, i, i, i, p, p, p, p, p, p, p, f, f, i, p, f, i, p, sz,
+                                      p], i),
         "nrc_query_status": ([p], i),
         "nrc_last_error_site": ([], i),
         "nrc_set_wait_timeout_ns": ([u64], None),
@@ -336,6 +339,16 @@ def linear_bn_swish_workspace_size(B, in_f, out_f) -> int:
     return int(load().nrc_linear_bn_swish_workspace_size(B, in_f, out_f))
 
 
+def _default_chunk_f(out_f):
+    return max(128, ((out_f + 3) // 4 + 127) // 128 * 128)
+
+
+def linear_bn_swish_host_workspace_size(B, in_f, out_f, chunk_f=None) -> int:
+    """Device workspace of the Linear on host buffers (x, weights and out in host memory)."""
+    return int(load().nrc_linear_bn_swish_host_workspace_size(
+        B, in_f, out_f, chunk_f or _default_chunk_f(out_f)))
+
+
 def linear_bn_swish(x, lin_weight, lin_bias, bn_gamma, bn_beta, bn_running_mean,
                     bn_running_var, add_bias, divide_value=1.0, bn_eps=1e-5, bn_momentum=0.1,
                     training=True, num_batches_tracked=None, out=None, workspace=None,
@@ -344,10 +357,17 @@ def linear_bn_swish(x, lin_weight, lin_bias, bn_gamma, bn_beta, bn_running_mean,
 
     In training mode bn_running_mean/var (device fp32 tensors) and
     num_batches_tracked (device int64 tensor or None) are updated in place.
-    add_bias is a one-element tensor (read on the device)."""
+    add_bias is a one-element tensor (read on the device).  With x in host
+    memory the call goes through nrc_linear_bn_swish_host (weights and
+    parameters taken to host memory, output in host memory; the stream is
+    synchronised before returning)."""
     lib = load()
     host = not x.is_cuda
     dev = _target_device(x)
+    if host:
+        return _linear_host(lib, dev, x, lin_weight, lin_bias, bn_gamma, bn_beta,
+                            bn_running_mean, bn_running_var, add_bias, divide_value, bn_eps,
+                            bn_momentum, training, num_batches_tracked, out, workspace, stream)
     xd = _dev(x, dev, torch.float32)
     B, IN = xd.shape
     w = _dev(lin_weight, dev, torch.float32)
@@ -375,6 +395,45 @@ def linear_bn_swish(x, lin_weight, lin_bias, bn_gamma, bn_beta, bn_running_mean,
         res.copy_(o)
         return res
     return o
+
+
+def _linear_host(lib, dev, x, w, lb, g, b, rm, rv, ab, divide_value, eps, momentum, training,
+                 nbt, out, workspace, stream, chunk_f=None):
+    """The Linear on host buffers through nrc_linear_bn_swish_host."""
+    if x.dtype != torch.float32:
+        raise TypeError("x must be fp32")
+    xh = x.contiguous()
+    B, IN = xh.shape
+    wh = _host(w, torch.float32)
+    OUT = wh.shape[0]
+    if wh.shape != (OUT, IN):
+        raise ValueError("lin_weight must be (out_features, in_features)")
+    lbh, gh, bh = (_host(t, torch.float32) for t in (lb, g, b))
+    abh = _host(torch.as_tensor(ab, dtype=torch.float32).reshape(1), torch.float32)
+    for t in (rm, rv):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and
+                t.numel() == OUT):
+            raise TypeError("running statistics must be contiguous fp32 device tensors")
+    if nbt is not None and not (nbt.is_cuda and nbt.dtype == torch.int64):
+        raise TypeError("num_batches_tracked must be an int64 device tensor")
+    chunk_f = chunk_f or _default_chunk_f(OUT)
+    need = lib.nrc_linear_bn_swish_host_workspace_size(B, IN, OUT, chunk_f)
+    if need == 0:
+        raise ValueError("bad shape for the host-buffer Linear")
+    ws = _workspace(need, dev, workspace)
+    res = out if out is not None else torch.empty((B, OUT), dtype=torch.float32,
+                                                  pin_memory=True)
+    if res.is_cuda or res.shape != (B, OUT) or res.dtype != torch.float32 or \
+            not res.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 (B, out_features) host tensor")
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    status = lib.nrc_linear_bn_swish_host(
+        _ptr(xh), _ptr(res), B, IN, OUT, _ptr(wh), _ptr(lbh), _ptr(gh), _ptr(bh), _ptr(rm),
+        _ptr(rv), _ptr(nbt), float(eps), float(momentum), int(bool(training)), _ptr(abh),
+        float(divide_value), int(chunk_f), _ptr(ws), ws.numel(), ctypes.c_void_p(st.cuda_stream))
+    _check(status, "nrc_linear_bn_swish_host")
+    st.synchronize()                      # out is host memory: valid on return
+    return res
 
 
 # ---------------------------------------------------------------------------

@@ -1331,32 +1331,6 @@ struct HostLayout {
     size_t par, w, b, x[2], o[2], total;
 };
 
-// The host entry's chunk sizes (samples): ramp-up chunk_n/4, chunk_n/2, then
-// chunk_n, then ramp-down chunk_n/2, chunk_n/4 (each at least 1; the last
-// middle chunk shorter if N asks).  chunk_n <= N.
-std::vector<int> host_chunk_sizes(int N, int chunk_n) {
-    const int r1 = std::max(1, chunk_n / 4), r2 = std::max(1, chunk_n / 2);
-    std::vector<int> sizes;
-    int rem = N;
-    auto push = [&](int t) {
-        if (t > 0) {
-            sizes.push_back(t);
-            rem -= t;
-        }
-    };
-    push(std::min(r1, rem));
-    push(std::min(r2, rem));
-    const int tail = std::min(rem, r1 + r2);
-    while (rem > tail) push(std::min(chunk_n, rem - tail));
-    if (tail > r1) {
-        push(tail - r1);
-        push(r1);
-    } else {
-        push(tail);
-    }
-    return sizes;
-}
-
 HostLayout host_layout(int N, int C, int L, nrc_dtype dt, int chunk_n) {
     const size_t es = dt == NRC_F32 ? 4 : 2;
     auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };

@@ -23,6 +23,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
+#include <vector>
 
 #include "nrc_launch.cuh"
 
@@ -352,38 +354,23 @@ static LinearPlan plan_linear(int B, int IN, int OUT, uint32_t x_box_bytes = 0) 
 
 using namespace nrc;
 
-extern "C" size_t nrc_linear_bn_swish_workspace_size(int B, int in_f, int out_f) {
-    if (B <= 0 || in_f <= 0 || out_f <= 0) return 0;
-    return plan_linear(B, in_f, out_f).total;
-}
+namespace {
 
-extern "C" nrc_status nrc_linear_bn_swish(
-    const float* x, float* out, int B, int in_f, int out_f, const float* lin_weight,
-    const float* lin_bias, const float* bn_gamma, const float* bn_beta, float* bn_running_mean,
-    float* bn_running_var, int64_t* num_batches_tracked, float bn_eps, float bn_momentum,
-    int training, const float* add_bias, float divide_value, void* workspace,
-    size_t workspace_bytes, void* stream) {
-    if (!x || !out || !lin_weight || !bn_running_mean || !bn_running_var || !add_bias ||
-        !workspace)
-        return NRC_ERR_INVALID_ARG;
-    if (B <= 0 || in_f <= 0 || out_f <= 0) return NRC_ERR_INVALID_ARG;
-    if ((bn_gamma == nullptr) != (bn_beta == nullptr)) return NRC_ERR_INVALID_ARG;
-    if (!(bn_eps >= 0.f) || !std::isfinite(bn_eps)) return NRC_ERR_INVALID_ARG;
-    if (!(bn_momentum >= 0.f && bn_momentum <= 1.f)) return NRC_ERR_INVALID_ARG;
-    if (divide_value == 0.f || !std::isfinite(divide_value)) return NRC_ERR_INVALID_ARG;
-    if (training != 0 && training != 1) return NRC_ERR_INVALID_ARG;
-    if (training && B < 2) return NRC_ERR_UNSUPPORTED;
-    if (ranges_overlap(x, (size_t)B * in_f * 4, out, (size_t)B * out_f * 4))
-        return NRC_ERR_INVALID_ARG;
-    if (!aligned(workspace, 256)) return NRC_ERR_ALIGNMENT;
+// The Linear chain on device buffers, x already packed at ws (the plan's
+// image): the GEMM, then in training mode the finalize and normalize kernels.
+// W, out and the per-feature arrays cover out_f features; num_batches_tracked
+// (NULL: not counted) is incremented by the finalize kernel.  b_after_prev:
+// the kernel just before on the stream wrote the x image.
+nrc_status linear_chain(const float* W, float* out, int B, int in_f, int out_f,
+                        const float* lin_bias, const float* bn_gamma, const float* bn_beta,
+                        float* bn_running_mean, float* bn_running_var,
+                        int64_t* num_batches_tracked, float bn_eps, float bn_momentum,
+                        int training, const float* add_bias, float divide_value, uint8_t* ws,
+                        bool b_after_prev, cudaStream_t st) {
     LinearPlan pl = plan_linear(B, in_f, out_f);
-    if (workspace_bytes < pl.total) return NRC_ERR_WORKSPACE;
     if ((long long)pl.n_jt * pl.n_bt >= (1LL << 30)) return NRC_ERR_UNSUPPORTED;
-
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
     LinearParams p{};
-    p.W = lin_weight;
+    p.W = W;
     p.xpack = ws;
     p.out = out;
     p.lin_bias = lin_bias;
@@ -395,15 +382,15 @@ extern "C" nrc_status nrc_linear_bn_swish(
     p.n_bt = pl.n_bt;
     p.n_kiters = pl.g.num_kiters;
     p.BN = pl.g.BN;
-    p.vec_ok = (in_f % 4 == 0) && aligned(lin_weight, 16);
+    p.vec_ok = (in_f % 4 == 0) && aligned(W, 16);
     // Staged A when W's rows are 16-byte aligned and the driver takes the map.
     bool staged = false;
     if (p.vec_ok) {
         const uint64_t dims[3] = {(uint64_t)in_f, (uint64_t)out_f, 1};
         const uint64_t strides[2] = {(uint64_t)in_f * 4, (uint64_t)in_f * 4 * out_f};
         const uint32_t box[3] = {32u, (uint32_t)kBM, 1u};
-        if (encode_tensor_map_3d(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, lin_weight, dims,
-                                 strides, box, false, true)) {
+        if (encode_tensor_map_3d(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W, dims, strides,
+                                 box, false, true)) {
             const LinearPlan ps = plan_linear(B, in_f, out_f, LinearProblem<true>::kBoxBytes);
             if (ps.g.b_stages >= 2 && ps.g.x_depth >= 2) {
                 pl = ps;
@@ -412,15 +399,7 @@ extern "C" nrc_status nrc_linear_bn_swish(
         }
     }
     float* colp = reinterpret_cast<float*>(ws + pl.colp_off);
-
-    const size_t units = (size_t)pl.n_bt * pl.g.num_kiters * pl.g.BN * 8;
-    {
-        TraceScope ts("pack_rows_split", st);
-        pack_rows_split_kernel<<<elementwise_grid(units), 256, 0, st>>>(
-            x, ws, B, in_f, pl.g.BN, pl.n_bt, pl.g.num_kiters);
-    }
-    if (cudaGetLastError() != cudaSuccess) return NRC_ERR_CUDA;
-    pl.g.b_after_prev = true;          // launched behind the x repack
+    pl.g.b_after_prev = b_after_prev;
     if (!training) {
         // eval: one GEMM whose epilogue writes out; the running statistics are
         // inputs here, so nothing else runs
@@ -460,4 +439,226 @@ extern "C" nrc_status nrc_linear_bn_swish(
         if (e != cudaSuccess) return cuda_status(e);
     }
     return cuda_status(cudaGetLastError());
+}
+
+// Packs x (B x in_f, device) into the workspace's x image.
+nrc_status linear_pack_x(const float* x, int B, int in_f, uint8_t* ws, cudaStream_t st) {
+    const LinearPlan pl = plan_linear(B, in_f, 1);
+    const size_t units = (size_t)pl.n_bt * pl.g.num_kiters * pl.g.BN * 8;
+    TraceScope ts("pack_rows_split", st);
+    pack_rows_split_kernel<<<elementwise_grid(units), 256, 0, st>>>(x, ws, B, in_f, pl.g.BN,
+                                                                     pl.n_bt, pl.g.num_kiters);
+    return cuda_status(cudaGetLastError());
+}
+
+// The argument checks shared by the device and host-buffer entries.
+nrc_status linear_check(const void* x, const void* out, int B, int in_f, int out_f,
+                        const void* lin_weight, const float* bn_gamma, const float* bn_beta,
+                        const float* bn_running_mean, const float* bn_running_var,
+                        float bn_eps, float bn_momentum, int training, const float* add_bias,
+                        float divide_value, const void* workspace) {
+    if (!x || !out || !lin_weight || !bn_running_mean || !bn_running_var || !add_bias ||
+        !workspace)
+        return NRC_ERR_INVALID_ARG;
+    if (B <= 0 || in_f <= 0 || out_f <= 0) return NRC_ERR_INVALID_ARG;
+    if ((bn_gamma == nullptr) != (bn_beta == nullptr)) return NRC_ERR_INVALID_ARG;
+    if (!(bn_eps >= 0.f) || !std::isfinite(bn_eps)) return NRC_ERR_INVALID_ARG;
+    if (!(bn_momentum >= 0.f && bn_momentum <= 1.f)) return NRC_ERR_INVALID_ARG;
+    if (divide_value == 0.f || !std::isfinite(divide_value)) return NRC_ERR_INVALID_ARG;
+    if (training != 0 && training != 1) return NRC_ERR_INVALID_ARG;
+    if (training && B < 2) return NRC_ERR_UNSUPPORTED;
+    if (ranges_overlap(x, (size_t)B * in_f * 4, out, (size_t)B * out_f * 4))
+        return NRC_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return NRC_ERR_ALIGNMENT;
+    return NRC_OK;
+}
+
+}  // namespace
+
+extern "C" size_t nrc_linear_bn_swish_workspace_size(int B, int in_f, int out_f) {
+    if (B <= 0 || in_f <= 0 || out_f <= 0) return 0;
+    return plan_linear(B, in_f, out_f).total;
+}
+
+extern "C" nrc_status nrc_linear_bn_swish(
+    const float* x, float* out, int B, int in_f, int out_f, const float* lin_weight,
+    const float* lin_bias, const float* bn_gamma, const float* bn_beta, float* bn_running_mean,
+    float* bn_running_var, int64_t* num_batches_tracked, float bn_eps, float bn_momentum,
+    int training, const float* add_bias, float divide_value, void* workspace,
+    size_t workspace_bytes, void* stream) {
+    const nrc_status c = linear_check(x, out, B, in_f, out_f, lin_weight, bn_gamma, bn_beta,
+                                      bn_running_mean, bn_running_var, bn_eps, bn_momentum,
+                                      training, add_bias, divide_value, workspace);
+    if (c != NRC_OK) return c;
+    if (workspace_bytes < plan_linear(B, in_f, out_f).total) return NRC_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const nrc_status s = linear_pack_x(x, B, in_f, ws, st);
+    if (s != NRC_OK) return s;
+    // launched behind the x repack
+    return linear_chain(lin_weight, out, B, in_f, out_f, lin_bias, bn_gamma, bn_beta,
+                        bn_running_mean, bn_running_var, num_batches_tracked, bn_eps,
+                        bn_momentum, training, add_bias, divide_value, ws, true, st);
+}
+
+// ---------------------------------------------------------------------------
+// Host-buffer entry: the output features in chunks (each feature's batch
+// statistics are independent of the others'), so the copy-in of the weight
+// rows of chunk j+1, the chain of chunk j and the copy-out of chunk j-1 run at
+// once.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct LinearHostLayout {
+    size_t xdev, par, w[2], o[2], total;
+};
+
+LinearHostLayout linear_host_layout(int B, int in_f, int out_f, int chunk_f) {
+    auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    LinearHostLayout h{};
+    h.xdev = up(plan_linear(B, in_f, chunk_f).total);
+    h.par = up(h.xdev + (size_t)B * in_f * 4);
+    h.w[0] = up(h.par + ((size_t)3 * out_f + 4) * 4);
+    h.w[1] = up(h.w[0] + (size_t)chunk_f * in_f * 4);
+    h.o[0] = up(h.w[1] + (size_t)chunk_f * in_f * 4);
+    h.o[1] = up(h.o[0] + (size_t)B * chunk_f * 4);
+    h.total = h.o[1] + (size_t)B * chunk_f * 4;
+    return h;
+}
+
+// Per device: the copy-in and copy-out streams and the events of the pipeline.
+struct LinearHostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start, join, ev_in[2], ev_chain[2], ev_out[2];
+    bool ready = false;
+};
+std::mutex g_lin_host_mu;
+LinearHostPipe g_lin_host_pipe[64];
+
+nrc_status linear_host_pipe(LinearHostPipe** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NRC_ERR_CUDA;
+    LinearHostPipe& hp = g_lin_host_pipe[dev];
+    if (!hp.ready) {
+        const unsigned f = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.start, f) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.join, f) != cudaSuccess)
+            return NRC_ERR_CUDA;
+        for (int b = 0; b < 2; ++b)
+            if (cudaEventCreateWithFlags(&hp.ev_in[b], f) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.ev_chain[b], f) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.ev_out[b], f) != cudaSuccess)
+                return NRC_ERR_CUDA;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return NRC_OK;
+}
+
+// chunk_f rounded to whole 128-feature tiles, at most out_f's tiles
+int linear_chunk_tiles(int out_f, int chunk_f) {
+    return std::max(1, std::min(ceil_div(out_f, kBM), ceil_div(chunk_f, kBM)));
+}
+
+}  // namespace
+
+extern "C" size_t nrc_linear_bn_swish_host_workspace_size(int B, int in_f, int out_f,
+                                                          int chunk_f) {
+    if (B <= 0 || in_f <= 0 || out_f <= 0 || chunk_f <= 0) return 0;
+    const int F = std::min(out_f, linear_chunk_tiles(out_f, chunk_f) * kBM);
+    return linear_host_layout(B, in_f, out_f, F).total;
+}
+
+extern "C" nrc_status nrc_linear_bn_swish_host(
+    const float* x_host, float* out_host, int B, int in_f, int out_f,
+    const float* lin_weight_host, const float* lin_bias_host, const float* bn_gamma_host,
+    const float* bn_beta_host, float* bn_running_mean, float* bn_running_var,
+    int64_t* num_batches_tracked, float bn_eps, float bn_momentum, int training,
+    const float* add_bias_host, float divide_value, int chunk_f, void* workspace,
+    size_t workspace_bytes, void* stream) {
+    const nrc_status c = linear_check(x_host, out_host, B, in_f, out_f, lin_weight_host,
+                                      bn_gamma_host, bn_beta_host, bn_running_mean,
+                                      bn_running_var, bn_eps, bn_momentum, training,
+                                      add_bias_host, divide_value, workspace);
+    if (c != NRC_OK) return c;
+    if (chunk_f <= 0) return NRC_ERR_INVALID_ARG;
+    const int tiles = ceil_div(out_f, kBM);
+    const int chunk_t = linear_chunk_tiles(out_f, chunk_f);
+    const int F = std::min(out_f, chunk_t * kBM);
+    const LinearHostLayout hl = linear_host_layout(B, in_f, out_f, F);
+    if (workspace_bytes < hl.total) return NRC_ERR_WORKSPACE;
+    if ((long long)tiles * kBM * in_f >= (1LL << 40)) return NRC_ERR_UNSUPPORTED;
+
+    std::lock_guard<std::mutex> lk(g_lin_host_mu);   // the per-device pipe is shared
+    LinearHostPipe* hp = nullptr;
+    nrc_status s = linear_host_pipe(&hp);
+    if (s != NRC_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // x and the per-feature parameters: copied on the caller's stream; x packed
+    // once for every chunk.
+    float* xdev = reinterpret_cast<float*>(ws + hl.xdev);
+    float* par = reinterpret_cast<float*>(ws + hl.par);
+    float* d_bias = par;
+    float* d_gamma = par + out_f;
+    float* d_beta = par + 2 * (size_t)out_f;
+    float* d_add = par + 3 * (size_t)out_f;
+    const size_t fb = (size_t)out_f * 4;
+    bool good = ok(cudaMemcpyAsync(xdev, x_host, (size_t)B * in_f * 4, cudaMemcpyHostToDevice,
+                                   st)) &&
+                ok(cudaMemcpyAsync(d_add, add_bias_host, 4, cudaMemcpyHostToDevice, st)) &&
+                (!lin_bias_host ||
+                 ok(cudaMemcpyAsync(d_bias, lin_bias_host, fb, cudaMemcpyHostToDevice, st))) &&
+                (!bn_gamma_host ||
+                 ok(cudaMemcpyAsync(d_gamma, bn_gamma_host, fb, cudaMemcpyHostToDevice, st))) &&
+                (!bn_beta_host ||
+                 ok(cudaMemcpyAsync(d_beta, bn_beta_host, fb, cudaMemcpyHostToDevice, st)));
+    if (!good) return NRC_ERR_CUDA;
+    s = linear_pack_x(xdev, B, in_f, ws, st);
+    if (s != NRC_OK) return s;
+    // The library streams start after everything already on the caller's stream
+    // (the workspace may still be in use by an earlier call).
+    if (!ok(cudaEventRecord(hp->start, st)) || !ok(cudaStreamWaitEvent(hp->in, hp->start, 0)) ||
+        !ok(cudaStreamWaitEvent(hp->out, hp->start, 0)))
+        return NRC_ERR_CUDA;
+    const std::vector<int> sizes = host_chunk_sizes(tiles, chunk_t);
+    const int n_chunks = (int)sizes.size();
+    int t0 = 0;
+    for (int j = 0; j < n_chunks; t0 += sizes[j], ++j) {
+        const int b = j & 1;
+        const int f0 = t0 * kBM;
+        const int fc = std::min(out_f - f0, sizes[j] * kBM);     // features of the chunk
+        float* wbuf = reinterpret_cast<float*>(ws + hl.w[b]);
+        float* obuf = reinterpret_cast<float*>(ws + hl.o[b]);
+        // copy-in of the chunk's weight rows: buffer b is free once chain j-2 ran
+        if (j >= 2 && !ok(cudaStreamWaitEvent(hp->in, hp->ev_chain[b], 0))) return NRC_ERR_CUDA;
+        if (!ok(cudaMemcpyAsync(wbuf, lin_weight_host + (size_t)f0 * in_f,
+                                (size_t)fc * in_f * 4, cudaMemcpyHostToDevice, hp->in)) ||
+            !ok(cudaEventRecord(hp->ev_in[b], hp->in)))
+            return NRC_ERR_CUDA;
+        // the chain: after its copy-in, and after chunk j-2's copy-out read buffer b
+        if (!ok(cudaStreamWaitEvent(st, hp->ev_in[b], 0)) ||
+            (j >= 2 && !ok(cudaStreamWaitEvent(st, hp->ev_out[b], 0))))
+            return NRC_ERR_CUDA;
+        s = linear_chain(wbuf, obuf, B, in_f, fc, lin_bias_host ? d_bias + f0 : nullptr,
+                         bn_gamma_host ? d_gamma + f0 : nullptr,
+                         bn_beta_host ? d_beta + f0 : nullptr, bn_running_mean + f0,
+                         bn_running_var + f0, j == 0 ? num_batches_tracked : nullptr, bn_eps,
+                         bn_momentum, training, d_add, divide_value, ws, false, st);
+        if (s != NRC_OK) return s;
+        if (!ok(cudaEventRecord(hp->ev_chain[b], st))) return NRC_ERR_CUDA;
+        // copy-out of the chunk's columns into the (B, out_f) rows
+        if (!ok(cudaStreamWaitEvent(hp->out, hp->ev_chain[b], 0)) ||
+            !ok(cudaMemcpy2DAsync(out_host + f0, fb, obuf, (size_t)fc * 4, (size_t)fc * 4, B,
+                                  cudaMemcpyDeviceToHost, hp->out)) ||
+            !ok(cudaEventRecord(hp->ev_out[b], hp->out)))
+            return NRC_ERR_CUDA;
+    }
+    // The caller's stream resumes once the last copy-out has landed.
+    if (!ok(cudaEventRecord(hp->join, hp->out)) || !ok(cudaStreamWaitEvent(st, hp->join, 0)))
+        return NRC_ERR_CUDA;
+    return NRC_OK;
 }

@@ -1,7 +1,9 @@
 // Host-side helpers shared by the translation units of libnrc.so.
 #pragma once
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -46,6 +48,35 @@ inline bool aligned(const void* p, size_t a) {
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 inline nrc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NRC_OK : NRC_ERR_CUDA; }
+
+// Chunk sizes of the host-buffer pipelines (in units: samples, or 128-feature
+// tiles): ramp-up chunk_n/4, chunk_n/2, then chunk_n, then ramp-down
+// chunk_n/2, chunk_n/4 (each at least 1; the last middle chunk shorter if N
+// asks), so the first copy-in and the last copy-out, which overlap nothing,
+// stay short.  chunk_n <= N.
+inline std::vector<int> host_chunk_sizes(int N, int chunk_n) {
+    const int r1 = std::max(1, chunk_n / 4), r2 = std::max(1, chunk_n / 2);
+    std::vector<int> sizes;
+    int rem = N;
+    auto push = [&](int t) {
+        if (t > 0) {
+            sizes.push_back(t);
+            rem -= t;
+        }
+    };
+    push(std::min(r1, rem));
+    push(std::min(r2, rem));
+    const int tail = std::min(rem, r1 + r2);
+    while (rem > tail) push(std::min(chunk_n, rem - tail));
+    if (tail > r1) {
+        push(tail - r1);
+        push(r1);
+    } else {
+        push(tail);
+    }
+    return sizes;
+}
+
 
 // Launch trace: when enabled (nrc_trace_enable), every kernel launch of the
 // library is bracketed by a pair of CUDA events recorded on its stream, so a

@@ -183,3 +183,49 @@ def test_back_to_back_calls_with_alternating_inputs():
     assert api.query_status() == api.NRC_OK
     for i, o in enumerate(outs):
         assert torch.equal(o, ref[i % 2]), f"call {i}"
+
+
+def _host_vs_device(dev, li, training, chunk_f):
+    """The host-buffer entry (chunked over output features) against the device
+    entry on the same inputs: bitwise equal outputs and running statistics."""
+    from normalization_convolution_blocks_gb300 import api
+    B, OUT = li.x.shape[0], li.weight.shape[0]
+    nbt_d = torch.zeros(1, dtype=torch.int64, device=dev)
+    rm_d, rv_d = to(dev, li.running_mean).clone(), to(dev, li.running_var).clone()
+    ref = api.linear_bn_swish(to(dev, li.x), to(dev, li.weight), to(dev, li.lin_bias),
+                              to(dev, li.gamma), to(dev, li.beta), rm_d, rv_d,
+                              to(dev, li.add_bias), li.divide_value, li.eps, li.momentum,
+                              training, nbt_d)
+    nbt_h = torch.zeros(1, dtype=torch.int64, device=dev)
+    rm_h, rv_h = to(dev, li.running_mean).clone(), to(dev, li.running_var).clone()
+    pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
+    out = torch.full((B, OUT), float("nan")).pin_memory()
+    got = api._linear_host(api.load(), dev, pin(li.x), pin(li.weight), pin(li.lin_bias),
+                           pin(li.gamma), pin(li.beta), rm_h, rv_h, pin(li.add_bias),
+                           li.divide_value, li.eps, li.momentum, training, nbt_h, out, None,
+                           None, chunk_f=chunk_f)
+    assert api.query_status() == api.NRC_OK
+    assert torch.equal(got, ref.cpu()), "host entry differs from the device entry"
+    assert torch.equal(rm_h, rm_d) and torch.equal(rv_h, rv_d), "running statistics differ"
+    assert int(nbt_h.item()) == int(nbt_d.item()) == (1 if training else 0)
+    return got
+
+
+@pytest.mark.parametrize("B,IN,OUT,chunk_f,training,affine", [
+    (300, 520, 1000, 256, True, True),     # ragged last chunk, ramped chunk sizes
+    (256, 1024, 2048, 512, False, True),   # eval mode
+    (64, 128, 130, 128, True, False),      # two tiles, the last chunk of 2 features
+    (33, 37, 50, 128, True, True),         # in_features % 4 != 0: W rows loaded directly
+])
+def test_host_buffer_entry_matches_device_entry(B, IN, OUT, chunk_f, training, affine):
+    dev = need_gpu()
+    li = syn.linear_bn_swish_inputs(B, IN, OUT, seed=B + OUT, random_affine=affine)
+    got = _host_vs_device(dev, li, training, chunk_f)
+    r_out = _ref(li, training)[0]
+    assert_f32(got.double().numpy(), r_out, f"host entry B{B} IN{IN} OUT{OUT}")
+
+
+def test_host_buffer_entry_full_workload():
+    dev = need_gpu()
+    li = syn.WORKLOADS["linear_bn_swish_f32"].make(seed=0)
+    _host_vs_device(dev, li, True, 2048)
