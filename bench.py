@@ -331,10 +331,12 @@ def make_call(name, dev, host=False):
         x, w, g, b = map(place, (inp.x, inp.weight, inp.gamma, inp.beta))
         N, Cin, T = x.shape
         Cout = w.shape[0]
-        out = None if host else torch.empty((N, Cout, T), device=dev)
-        ws = None if host else torch.empty(
-            api.conv1d_groupnorm_workspace_size(N, Cin, Cout, T, inp.num_groups),
-            dtype=torch.uint8, device=dev)
+        # host buffers: the output is pinned and the workspace allocated once
+        out = torch.empty((N, Cout, T), pin_memory=True) if host else \
+            torch.empty((N, Cout, T), device=dev)
+        ws_bytes = api.conv1d_groupnorm_host_workspace_size(N, Cin, Cout, T, inp.num_groups) \
+            if host else api.conv1d_groupnorm_workspace_size(N, Cin, Cout, T, inp.num_groups)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         tensors_in = (x, w, g, b)
 
         def call():

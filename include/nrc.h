@@ -242,6 +242,42 @@ nrc_status nrc_conv1d_groupnorm(
     void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Conv1d + GroupNorm on HOST buffers (end-to-end path).  The pages have no
+ * counterpart: a library convenience.
+ *
+ * Same computation, arguments and errors as nrc_conv1d_groupnorm, with
+ * x_host, out_host, conv_weight_host, conv_bias_host, gn_gamma_host and
+ * gn_beta_host in HOST memory (pinned for the copies to overlap).  A sample's
+ * group statistics involve that sample alone, so the batch runs in chunks of
+ * chunk_n samples (the last one smaller if N asks): the parameters are copied
+ * once, then the copy-in of chunk j+1, nrc_conv1d_groupnorm on chunk j and the
+ * copy-out of chunk j-1 run at once, on two library-owned streams and
+ * `stream`, ordered by events.  Each chunk is an ordinary device-entry call on
+ * its samples: the results are bitwise those of the device entry on the whole
+ * batch when both take the same kernel path, and agree to rounding otherwise
+ * (a chunk whose tiles fit one wave takes the fused one-kernel path where the
+ * whole batch may not).
+ * workspace: DEVICE memory, 256-byte aligned, of at least
+ *   nrc_conv1d_groupnorm_host_workspace_size(..., chunk_n) bytes (the device
+ *   entry's workspace for one chunk, the parameters, two x and two out chunk
+ *   buffers); 0 from the query: invalid arguments.  chunk_n <= 0 returns
+ *   NRC_ERR_INVALID_ARG.
+ * Asynchronous: work already on `stream` comes first; `stream` resumes after
+ * the last copy-out, so synchronising `stream` makes out_host valid.  Calls
+ * from several host threads are serialised inside the library.
+ * ------------------------------------------------------------------------ */
+size_t nrc_conv1d_groupnorm_host_workspace_size(int N, int C_in, int C_out, int T,
+                                                int kernel_size, int stride, int padding,
+                                                int dilation, int num_groups, int chunk_n);
+
+nrc_status nrc_conv1d_groupnorm_host(
+    const float *x_host, float *out_host, int N, int C_in, int C_out, int T,
+    int kernel_size, int stride, int padding, int dilation,
+    const float *conv_weight_host, const float *conv_bias_host,
+    int num_groups, const float *gn_gamma_host, const float *gn_beta_host, float eps,
+    int chunk_n, void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Linear + BatchNorm1d + scalar bias + divide + Swish ("Kimi-K2.6 l2_p97")
  *
  *   y = x W^T + lin_bias                                 (B x out_f)

@@ -67,6 +67,9 @@ def load() -> ctypes.CDLL:
         "nrc_conv1d_output_length": ([i, i, i, i, i], i),
         "nrc_conv1d_groupnorm_workspace_size": ([i, i, i, i, i, i, i, i, i], sz),
         "nrc_conv1d_groupnorm": ([p, p, i, i, i, i, i, i, i, i, p, p, i, p, p, f, p, sz, p], i),
+        "nrc_conv1d_groupnorm_host_workspace_size": ([i, i, i, i, i, i, i, i, i, i], sz),
+        "nrc_conv1d_groupnorm_host": ([p, p, i, i, i, i, i, i, i, i, p, p, i, p, p, f, i, p, sz,
+                                       p], i),
         "nrc_linear_bn_swish_workspace_size": ([i, i, i], sz),
         "nrc_linear_bn_swish": ([p, p, i, i, i, p, p, p, p, p, p, p, f, f, i, p, f, p, sz, p], i),
         "nrc_linear_bn_swish_host_workspace_size": ([i, i, i, i], sz),
@@ -297,10 +300,16 @@ def conv1d_groupnorm(x, conv_weight, conv_bias, num_groups, gn_gamma, gn_beta, e
                      kernel_size=None, stride=1, padding=1, dilation=1, out=None, workspace=None,
                      stream=None):
     """GroupNorm(num_groups)(Conv1d(x)); x (N, C_in, T) fp32, conv_weight
-    (C_out, C_in, kernel_size); the result is (N, C_out, T_out)."""
+    (C_out, C_in, kernel_size); the result is (N, C_out, T_out).  With x in
+    host memory the call goes through nrc_conv1d_groupnorm_host (parameters
+    taken to host memory, output in host memory; the stream is synchronised
+    before returning)."""
     lib = load()
     host = not x.is_cuda
     dev = _target_device(x)
+    if host:
+        return _gn_host(lib, dev, x, conv_weight, conv_bias, num_groups, gn_gamma, gn_beta, eps,
+                        kernel_size, stride, padding, dilation, out, workspace, stream)
     xd = _dev(x, dev, torch.float32)
     N, Cin, T = xd.shape
     w = _dev(conv_weight, dev, torch.float32)
@@ -330,6 +339,52 @@ def conv1d_groupnorm(x, conv_weight, conv_bias, num_groups, gn_gamma, gn_beta, e
         res.copy_(o)
         return res
     return o
+
+
+def _gn_host(lib, dev, x, w, cb, G, g, b, eps, kernel_size, stride, padding, dilation, out,
+             workspace, stream, chunk_n=None):
+    """Conv1d + GroupNorm on host buffers through nrc_conv1d_groupnorm_host."""
+    if x.dtype != torch.float32:
+        raise TypeError("x must be fp32")
+    xh = x.contiguous()
+    N, Cin, T = xh.shape
+    wh = _host(w, torch.float32)
+    Cout = wh.shape[0]
+    if kernel_size is None:
+        kernel_size = wh.shape[2]
+    if wh.dim() != 3 or wh.shape[1] != Cin or wh.shape[2] != kernel_size:
+        raise ValueError("conv_weight must be (C_out, C_in, kernel_size)")
+    T_out = int(lib.nrc_conv1d_output_length(T, kernel_size, stride, padding, dilation))
+    if T_out <= 0:
+        raise ValueError("the conv's kernel does not fit the padded input")
+    cbh, gh, bh = (_host(t, torch.float32) for t in (cb, g, b))
+    chunk_n = chunk_n or (N + 1) // 2
+    need = lib.nrc_conv1d_groupnorm_host_workspace_size(N, Cin, Cout, T, kernel_size, stride,
+                                                        padding, dilation, G, chunk_n)
+    if need == 0:
+        raise ValueError("bad arguments for the host-buffer Conv1d + GroupNorm")
+    ws = _workspace(need, dev, workspace)
+    res = out if out is not None else torch.empty((N, Cout, T_out), dtype=torch.float32,
+                                                  pin_memory=True)
+    if res.is_cuda or res.shape != (N, Cout, T_out) or res.dtype != torch.float32 or \
+            not res.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 (N, C_out, T_out) host tensor")
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    status = lib.nrc_conv1d_groupnorm_host(
+        _ptr(xh), _ptr(res), N, Cin, Cout, T, kernel_size, stride, padding, dilation, _ptr(wh),
+        _ptr(cbh), G, _ptr(gh), _ptr(bh), float(eps), int(chunk_n), _ptr(ws), ws.numel(),
+        ctypes.c_void_p(st.cuda_stream))
+    _check(status, "nrc_conv1d_groupnorm_host")
+    st.synchronize()                      # out is host memory: valid on return
+    return res
+
+
+def conv1d_groupnorm_host_workspace_size(N, C_in, C_out, T, num_groups, kernel_size=3, stride=1,
+                                         padding=1, dilation=1, chunk_n=None) -> int:
+    """Device workspace of Conv1d + GroupNorm on host buffers."""
+    return int(load().nrc_conv1d_groupnorm_host_workspace_size(
+        N, C_in, C_out, T, kernel_size, stride, padding, dilation, num_groups,
+        chunk_n or (N + 1) // 2))
 
 
 # ---------------------------------------------------------------------------

@@ -1520,13 +1520,14 @@ extern "C" size_t nrc_conv1d_groupnorm_workspace_size(int N, int C_in, int C_out
     return gn_partials_offset(pl) + (size_t)N * num_groups * pl.n_tt * kBM * sizeof(float2);
 }
 
-extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, int C_in, int C_out,
-                                           int T, int kernel_size, int stride, int padding,
-                                           int dilation, const float* conv_weight,
-                                           const float* conv_bias, int num_groups,
-                                           const float* gn_gamma, const float* gn_beta, float eps,
-                                           void* workspace, size_t workspace_bytes,
-                                           void* stream) {
+namespace {
+
+// The argument checks of the Conv1d + GroupNorm entries (device and host
+// buffers alike); T_out receives the conv's output length.
+nrc_status gn_check(const void* x, const void* out, int N, int C_in, int C_out, int T,
+                    int kernel_size, int stride, int padding, int dilation,
+                    const void* conv_weight, int num_groups, const float* gn_gamma,
+                    const float* gn_beta, float eps, const void* workspace, int* T_out_p) {
     if (!x || !out || !conv_weight || !workspace) return NRC_ERR_INVALID_ARG;
     if (N <= 0 || C_in <= 0 || C_out <= 0 || T <= 0 || num_groups <= 0)
         return NRC_ERR_INVALID_ARG;
@@ -1546,6 +1547,25 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
     if (ranges_overlap(x, (size_t)N * C_in * T * 4, out, (size_t)N * C_out * T_out * 4))
         return NRC_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return NRC_ERR_ALIGNMENT;
+    *T_out_p = T_out;
+    return NRC_OK;
+}
+
+}  // namespace
+
+extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, int C_in, int C_out,
+                                           int T, int kernel_size, int stride, int padding,
+                                           int dilation, const float* conv_weight,
+                                           const float* conv_bias, int num_groups,
+                                           const float* gn_gamma, const float* gn_beta, float eps,
+                                           void* workspace, size_t workspace_bytes,
+                                           void* stream) {
+    int T_out = 0;
+    const nrc_status chk = gn_check(x, out, N, C_in, C_out, T, kernel_size, stride, padding,
+                                    dilation, conv_weight, num_groups, gn_gamma, gn_beta, eps,
+                                    workspace, &T_out);
+    if (chk != NRC_OK) return chk;
+    const int cpg = C_out / num_groups;
     ConvPlan pl = plan_conv(N, C_in, C_out, T_out, 2, false, 0, 0, kernel_size);
     if (workspace_bytes < nrc_conv1d_groupnorm_workspace_size(N, C_in, C_out, T, kernel_size,
                                                               stride, padding, dilation,
@@ -1636,6 +1656,139 @@ extern "C" nrc_status nrc_conv1d_groupnorm(const float* x, float* out, int N, in
             out, p.partials, pl.n_tt, C_out, T_out, num_groups, gn_gamma, gn_beta, eps);
     }
     return cuda_status(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// Conv1d + GroupNorm on host buffers: the batch in chunks of samples (a
+// sample's group statistics involve that sample alone), so the copy-in of
+// chunk j+1, the call on chunk j and the copy-out of chunk j-1 run at once.
+// Each chunk is an ordinary call of the device entry on its samples.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct GnHostLayout {
+    size_t par_w, par_b, par_g, par_be, x[2], o[2], total;
+};
+
+GnHostLayout gn_host_layout(int C_in, int C_out, int T, int T_out, int kernel_size,
+                            size_t gn_ws, int chunk_n) {
+    auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    GnHostLayout h{};
+    h.par_w = up(gn_ws);
+    h.par_b = up(h.par_w + (size_t)C_out * C_in * kernel_size * 4);
+    h.par_g = up(h.par_b + (size_t)C_out * 4);
+    h.par_be = up(h.par_g + (size_t)C_out * 4);
+    h.x[0] = up(h.par_be + (size_t)C_out * 4);
+    h.x[1] = up(h.x[0] + (size_t)chunk_n * C_in * T * 4);
+    h.o[0] = up(h.x[1] + (size_t)chunk_n * C_in * T * 4);
+    h.o[1] = up(h.o[0] + (size_t)chunk_n * C_out * T_out * 4);
+    h.total = h.o[1] + (size_t)chunk_n * C_out * T_out * 4;
+    return h;
+}
+
+}  // namespace
+
+extern "C" size_t nrc_conv1d_groupnorm_host_workspace_size(int N, int C_in, int C_out, int T,
+                                                           int kernel_size, int stride,
+                                                           int padding, int dilation,
+                                                           int num_groups, int chunk_n) {
+    if (N <= 0 || chunk_n <= 0) return 0;
+    chunk_n = std::min(chunk_n, N);
+    const size_t gn_ws = nrc_conv1d_groupnorm_workspace_size(chunk_n, C_in, C_out, T, kernel_size,
+                                                             stride, padding, dilation,
+                                                             num_groups);
+    if (gn_ws == 0) return 0;
+    const int T_out = nrc_conv1d_output_length(T, kernel_size, stride, padding, dilation);
+    return gn_host_layout(C_in, C_out, T, T_out, kernel_size, gn_ws, chunk_n).total;
+}
+
+extern "C" nrc_status nrc_conv1d_groupnorm_host(
+    const float* x_host, float* out_host, int N, int C_in, int C_out, int T, int kernel_size,
+    int stride, int padding, int dilation, const float* conv_weight_host,
+    const float* conv_bias_host, int num_groups, const float* gn_gamma_host,
+    const float* gn_beta_host, float eps, int chunk_n, void* workspace, size_t workspace_bytes,
+    void* stream) {
+    int T_out = 0;
+    const nrc_status chk = gn_check(x_host, out_host, N, C_in, C_out, T, kernel_size, stride,
+                                    padding, dilation, conv_weight_host, num_groups,
+                                    gn_gamma_host, gn_beta_host, eps, workspace, &T_out);
+    if (chk != NRC_OK) return chk;
+    if (chunk_n <= 0) return NRC_ERR_INVALID_ARG;
+    chunk_n = std::min(chunk_n, N);
+    const size_t gn_ws = nrc_conv1d_groupnorm_workspace_size(chunk_n, C_in, C_out, T, kernel_size,
+                                                             stride, padding, dilation,
+                                                             num_groups);
+    if (gn_ws == 0) return NRC_ERR_INVALID_ARG;
+    const GnHostLayout hl = gn_host_layout(C_in, C_out, T, T_out, kernel_size, gn_ws, chunk_n);
+    if (workspace_bytes < hl.total) return NRC_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return NRC_ERR_ALIGNMENT;
+
+    std::lock_guard<std::mutex> lk(g_host_mu);      // the per-device pipe is shared
+    HostPipe* hp = nullptr;
+    nrc_status s = host_pipe(&hp);
+    if (s != NRC_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // Weights and affine parameters: copied once on the caller's stream.
+    float* d_w = reinterpret_cast<float*>(ws + hl.par_w);
+    float* d_b = reinterpret_cast<float*>(ws + hl.par_b);
+    float* d_g = reinterpret_cast<float*>(ws + hl.par_g);
+    float* d_be = reinterpret_cast<float*>(ws + hl.par_be);
+    const size_t cb = (size_t)C_out * 4;
+    const bool good =
+        ok(cudaMemcpyAsync(d_w, conv_weight_host, (size_t)C_out * C_in * kernel_size * 4,
+                           cudaMemcpyHostToDevice, st)) &&
+        (!conv_bias_host || ok(cudaMemcpyAsync(d_b, conv_bias_host, cb, cudaMemcpyHostToDevice,
+                                               st))) &&
+        (!gn_gamma_host || ok(cudaMemcpyAsync(d_g, gn_gamma_host, cb, cudaMemcpyHostToDevice,
+                                              st))) &&
+        (!gn_beta_host ||
+         ok(cudaMemcpyAsync(d_be, gn_beta_host, cb, cudaMemcpyHostToDevice, st)));
+    if (!good) return NRC_ERR_CUDA;
+    // The library streams start after everything already on the caller's stream.
+    if (!ok(cudaEventRecord(hp->start, st)) || !ok(cudaStreamWaitEvent(hp->in, hp->start, 0)) ||
+        !ok(cudaStreamWaitEvent(hp->out, hp->start, 0)))
+        return NRC_ERR_CUDA;
+    const size_t xs = (size_t)C_in * T * 4, os = (size_t)C_out * T_out * 4;   // per sample
+    // Equal chunks, no ramp: a call costs about the same whatever its size (the
+    // kernel is latency-bound), so fewer calls beat shorter first and last copies.
+    std::vector<int> sizes;
+    for (int r = N; r > 0; r -= chunk_n) sizes.push_back(std::min(chunk_n, r));
+    const int n_chunks = (int)sizes.size();
+    int n0 = 0;
+    for (int j = 0; j < n_chunks; n0 += sizes[j], ++j) {
+        const int b = j & 1;
+        const int cn = sizes[j];
+        // copy-in: buffer b is free once the call on chunk j-2 has read it
+        if (j >= 2 && !ok(cudaStreamWaitEvent(hp->in, hp->ev_gemm[b], 0))) return NRC_ERR_CUDA;
+        if (!ok(cudaMemcpyAsync(ws + hl.x[b], reinterpret_cast<const uint8_t*>(x_host) + n0 * xs,
+                                (size_t)cn * xs, cudaMemcpyHostToDevice, hp->in)) ||
+            !ok(cudaEventRecord(hp->ev_in[b], hp->in)))
+            return NRC_ERR_CUDA;
+        // the call: after its copy-in, and after chunk j-2's copy-out read buffer b
+        if (!ok(cudaStreamWaitEvent(st, hp->ev_in[b], 0)) ||
+            (j >= 2 && !ok(cudaStreamWaitEvent(st, hp->ev_out[b], 0))))
+            return NRC_ERR_CUDA;
+        s = nrc_conv1d_groupnorm(reinterpret_cast<const float*>(ws + hl.x[b]),
+                                 reinterpret_cast<float*>(ws + hl.o[b]), cn, C_in, C_out, T,
+                                 kernel_size, stride, padding, dilation, d_w,
+                                 conv_bias_host ? d_b : nullptr, num_groups,
+                                 gn_gamma_host ? d_g : nullptr, gn_beta_host ? d_be : nullptr,
+                                 eps, ws, gn_ws, stream);
+        if (s != NRC_OK) return s;
+        if (!ok(cudaEventRecord(hp->ev_gemm[b], st))) return NRC_ERR_CUDA;
+        // copy-out
+        if (!ok(cudaStreamWaitEvent(hp->out, hp->ev_gemm[b], 0)) ||
+            !ok(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out_host) + n0 * os, ws + hl.o[b],
+                                (size_t)cn * os, cudaMemcpyDeviceToHost, hp->out)) ||
+            !ok(cudaEventRecord(hp->ev_out[b], hp->out)))
+            return NRC_ERR_CUDA;
+    }
+    // The caller's stream resumes once the last copy-out has landed.
+    if (!ok(cudaEventRecord(hp->join, hp->out)) || !ok(cudaStreamWaitEvent(st, hp->join, 0)))
+        return NRC_ERR_CUDA;
+    return NRC_OK;
 }
 
 // ---------------------------------------------------------------------------

@@ -142,3 +142,43 @@ def test_general_conv_with_bias_and_unaligned_rows():
     bias = torch.linspace(-0.5, 0.5, 48)
     kw = dict(bias=bias, stride=1, padding=3, dilation=2)
     assert_f32(_gpu(dev, g, 6, **kw), _ref(g, 6, **kw), "k5 d2 p3 T301 with bias")
+
+
+@pytest.mark.parametrize("N,Cin,Cout,T,G,k,s,p,d,chunk_n,affine,bias", [
+    (16, 128, 256, 1024, 32, 3, 1, 1, 1, 4, True, False),    # the workload, chunks of 4
+    (7, 64, 40, 1000, 5, 3, 1, 1, 1, 2, True, True),         # ragged chunks, conv bias
+    (5, 32, 64, 300, 8, 5, 3, 4, 2, 3, False, False),        # general conv, no affine
+    (6, 64, 128, 4096, 16, 3, 1, 1, 1, 6, True, False),      # 192 tiles: the multi-wave path
+])
+def test_host_buffer_entry_matches_device_entry(N, Cin, Cout, T, G, k, s, p, d, chunk_n, affine,
+                                                bias):
+    """The host-buffer entry (chunks of samples) against the device entry:
+    bitwise equal, and within the fp32 bar of the oracle."""
+    dev = need_gpu()
+    from normalization_convolution_blocks_gb300 import api
+    g = syn.conv_groupnorm_inputs(N, Cin, Cout, T, G, seed=N + Cin + T, kernel_size=k)
+    cb = torch.rand(Cout) - 0.5 if bias else None
+    ref = api.conv1d_groupnorm(to(dev, g.x), to(dev, g.weight), to(dev, cb), G,
+                               to(dev, g.gamma) if affine else None,
+                               to(dev, g.beta) if affine else None, g.eps, stride=s, padding=p,
+                               dilation=d)
+    pin = lambda t: None if t is None else t.contiguous().pin_memory()  # noqa: E731
+    T_out = api.conv1d_output_length(T, k, s, p, d)
+    out = torch.full((N, Cout, T_out), float("nan")).pin_memory()
+    got = api._gn_host(api.load(), dev, pin(g.x), pin(g.weight), pin(cb), G,
+                       pin(g.gamma) if affine else None, pin(g.beta) if affine else None, g.eps,
+                       None, s, p, d, out, None, None, chunk_n=chunk_n)
+    assert api.query_status() == api.NRC_OK
+    tiles = N * -(-api.conv1d_output_length(T, k, s, p, d) // 128) * -(-Cout // 256)
+    if tiles <= torch.cuda.get_device_properties(dev).multi_processor_count:
+        # the whole batch fits one wave, so every chunk does too: the same fused
+        # kernel path, bitwise equal
+        assert torch.equal(got, ref.cpu()), "host entry differs from the device entry"
+    else:
+        # the whole batch takes the multi-wave path, a chunk may take the fused
+        # one: the group statistics are summed in another order
+        assert (got - ref.cpu()).abs().max().item() < 1e-5, "host entry far from the device entry"
+    want = oracle.conv_groupnorm(g.x, g.weight, cb, G, g.gamma if affine else None,
+                                 g.beta if affine else None, g.eps, stride=s, padding=p,
+                                 dilation=d)
+    assert_f32(got.double().numpy(), want, f"host entry N{N} {Cin}->{Cout} T{T}")
