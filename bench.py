@@ -316,9 +316,12 @@ def make_call(name, dev, host=False):
         x, g, b, w, bias = map(place, (inp.x, inp.gamma, inp.beta, inp.weight, inp.bias))
         rm, rv = inp.running_mean.to(dev), inp.running_var.to(dev)
         nbt = torch.zeros(1, dtype=torch.int64, device=dev)
-        out = None if host else torch.empty_like(x)
-        ws = torch.empty(api.prenorm_dilconv_residual_train_workspace_size(*x.shape, x.dtype),
-                         dtype=torch.uint8, device=dev)
+        # host buffers: the output is pinned and the workspace allocated once
+        out = torch.empty(x.shape, dtype=x.dtype, pin_memory=True) if host else \
+            torch.empty_like(x)
+        ws_bytes = api.prenorm_dilconv_residual_train_host_workspace_size(*x.shape, x.dtype) \
+            if host else api.prenorm_dilconv_residual_train_workspace_size(*x.shape, x.dtype)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         tensors_in = (x, g, b, w, bias)
 
         def call():

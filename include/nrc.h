@@ -134,6 +134,38 @@ nrc_status nrc_prenorm_dilconv_residual_train(
     const void *conv_weight, const void *conv_bias,
     void *workspace, size_t workspace_bytes, void *stream);
 
+/* Training-mode block on HOST buffers (end-to-end path; a library
+ * convenience, the pages have no counterpart).  Same computation, arguments
+ * and errors as nrc_prenorm_dilconv_residual_train, with x_host, out_host,
+ * bn_gamma_host, bn_beta_host, conv_weight_host and conv_bias_host in HOST
+ * memory (pinned for the copies to overlap), while the running buffers and
+ * num_batches_tracked stay DEVICE buffers updated in place.  The batch
+ * statistics need every sample first, so the chunks of chunk_n samples (first
+ * and last smaller) go through two phases: x is copied into one device copy
+ * of the whole batch chunk by chunk, each chunk's row statistics computed
+ * behind its copy; after the merge, the block runs on chunk j while chunk
+ * j-1's output is copied out.  Two library-owned streams and `stream`,
+ * ordered by events.  Results are those of the device entry on the whole batch
+ * (the statistics merge in the same order; each chunk's block call uses the
+ * one-wave or multi-wave kernel its size asks for, which give bitwise equal
+ * results).
+ * workspace: DEVICE memory, 256-byte aligned, of at least
+ *   nrc_prenorm_dilconv_residual_train_host_workspace_size(N, C, L, dt,
+ *   chunk_n) bytes (the device entry's workspace, a device copy of x, two out
+ *   chunk buffers and the parameters); chunk_n <= 0 returns
+ *   NRC_ERR_INVALID_ARG.  Asynchronous: synchronising `stream` makes out_host
+ *   valid.  Calls from several host threads are serialised inside the library. */
+size_t nrc_prenorm_dilconv_residual_train_host_workspace_size(int N, int C, int L, nrc_dtype dt,
+                                                              int chunk_n);
+
+nrc_status nrc_prenorm_dilconv_residual_train_host(
+    const void *x_host, void *out_host, nrc_dtype dt, int N, int C, int L,
+    int kernel_size, int dilation, int padding,
+    float *bn_running_mean, float *bn_running_var, long long *num_batches_tracked,
+    const float *bn_gamma_host, const float *bn_beta_host, float bn_eps, float bn_momentum,
+    const void *conv_weight_host, const void *conv_bias_host, int chunk_n,
+    void *workspace, size_t workspace_bytes, void *stream);
+
 /* ------------------------------------------------------------------------
  * Pre-norm residual block on HOST buffers.  Same computation and errors as
  * nrc_prenorm_dilconv_residual ("Kimi-K2.6 l2_p12", problem statement), for

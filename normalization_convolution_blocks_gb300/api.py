@@ -58,6 +58,9 @@ def load() -> ctypes.CDLL:
         "nrc_prenorm_dilconv_residual_train_workspace_size": ([i, i, i, i], sz),
         "nrc_prenorm_dilconv_residual_train": ([p, p, i, i, i, i, i, i, i, p, p, p, p, p, f, f, p,
                                                 p, p, sz, p], i),
+        "nrc_prenorm_dilconv_residual_train_host_workspace_size": ([i, i, i, i, i], sz),
+        "nrc_prenorm_dilconv_residual_train_host": ([p, p, i, i, i, i, i, i, i, p, p, p, p, p, f,
+                                                     f, p, p, i, p, sz, p], i),
         "nrc_prenorm_dilconv_residual_host_workspace_size": ([i, i, i, i, i], sz),
         "nrc_prenorm_dilconv_residual_host": ([p, p, i, i, i, i, i, i, i, p, p, p, p, f, p, p, i,
                                                p, sz, p], i),
@@ -194,8 +197,10 @@ def prenorm_dilconv_residual_train(x, bn_running_mean, bn_running_var, bn_gamma,
     own per-channel mean and biased variance over (N, L), and the running
     buffers (contiguous fp32 device tensors, or None) are updated in place
     with the unbiased variance; num_batches_tracked (an int64 device tensor
-    or None) is incremented.  With x in host memory it is copied in, and the
-    result comes back as a host tensor (pinned)."""
+    or None) is incremented.  With x in host memory the call goes through
+    nrc_prenorm_dilconv_residual_train_host (parameters taken to host memory,
+    the result a pinned host tensor; the stream is synchronised before
+    returning)."""
     lib = load()
     if x.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("x must be float32 or bfloat16")
@@ -208,6 +213,10 @@ def prenorm_dilconv_residual_train(x, bn_running_mean, bn_running_var, bn_gamma,
     if num_batches_tracked is not None and not (num_batches_tracked.is_cuda and
                                                 num_batches_tracked.dtype == torch.int64):
         raise TypeError("num_batches_tracked must be an int64 device tensor")
+    if host:
+        return _train_host(lib, dev, dt, x, bn_running_mean, bn_running_var, bn_gamma, bn_beta,
+                           bn_eps, bn_momentum, conv_weight, conv_bias, dilation, padding,
+                           kernel_size, num_batches_tracked, out, workspace, stream)
     xd = _dev(x, dev)
     N, C, L = xd.shape
     g, b = (_dev(t, dev, torch.float32) for t in (bn_gamma, bn_beta))
@@ -228,6 +237,41 @@ def prenorm_dilconv_residual_train(x, bn_running_mean, bn_running_var, bn_gamma,
         res.copy_(o)
         return res
     return o
+
+
+def _train_host(lib, dev, dt, x, rm, rv, g, b, eps, momentum, w, cb, dilation, padding,
+                kernel_size, nbt, out, workspace, stream, chunk_n=None):
+    """The training-mode block on host buffers through
+    nrc_prenorm_dilconv_residual_train_host."""
+    xh = x.contiguous()
+    N, C, L = xh.shape
+    gh, bh = (_host(t, torch.float32) for t in (g, b))
+    wh, cbh = _host(w, x.dtype), _host(cb, x.dtype)
+    padding = dilation if padding is None else padding
+    chunk_n = chunk_n or _default_chunk(N)
+    need = lib.nrc_prenorm_dilconv_residual_train_host_workspace_size(N, C, L, dt, chunk_n)
+    if need == 0:
+        raise ValueError("bad shape for the host-buffer training-mode block")
+    ws = _workspace(need, dev, workspace)
+    res = out if out is not None else torch.empty(xh.shape, dtype=xh.dtype, pin_memory=True)
+    if res.is_cuda or res.shape != xh.shape or res.dtype != xh.dtype or not res.is_contiguous():
+        raise ValueError("out must be a contiguous host tensor of x's shape and dtype")
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    status = lib.nrc_prenorm_dilconv_residual_train_host(
+        _ptr(xh), _ptr(res), dt, N, C, L, kernel_size, dilation, padding, _ptr(rm), _ptr(rv),
+        _ptr(nbt), _ptr(gh), _ptr(bh), float(eps), float(momentum), _ptr(wh), _ptr(cbh),
+        int(chunk_n), _ptr(ws), ws.numel(), ctypes.c_void_p(st.cuda_stream))
+    _check(status, "nrc_prenorm_dilconv_residual_train_host")
+    st.synchronize()                      # out is host memory: valid on return
+    return res
+
+
+def prenorm_dilconv_residual_train_host_workspace_size(N, C, L, dtype=torch.float32,
+                                                       chunk_n=None) -> int:
+    """Device workspace of the training-mode block on host buffers."""
+    dt = NRC_F32 if dtype == torch.float32 else NRC_BF16
+    return int(load().nrc_prenorm_dilconv_residual_train_host_workspace_size(
+        N, C, L, dt, chunk_n or _default_chunk(N)))
 
 
 def prenorm_dilconv_residual_host_workspace_size(N, C, L, dtype=torch.float32,

@@ -165,3 +165,36 @@ def test_three_steps_track_the_oracle():
     _check_buffers(rm.double().cpu().numpy(), rv.double().cpu().numpy(), ref_rm, ref_rv,
                    "three steps")
     assert int(nbt.item()) == 3
+
+
+@pytest.mark.parametrize("N,C,L,d,chunk_n,dtype", [
+    (8, 64, 1000, 16, 2, torch.float32),      # ramped chunks 1,1,2,2,1,1 ... of a small batch
+    (5, 96, 2048, 128, 2, torch.bfloat16),    # bf16, ragged chunking
+    (3, 32, 300, 7, 1, torch.float32),        # L % 4 != 0: scalar statistics loads
+    (32, 256, 4096, 128, 4, torch.float32),   # the full workload
+])
+def test_host_buffer_entry_matches_device_entry(N, C, L, d, chunk_n, dtype):
+    """The host-buffer entry (statistics per chunk as x arrives, then the block
+    per chunk) against the device entry on the whole batch: bitwise equal
+    output, running buffers and num_batches_tracked."""
+    dev = need_gpu()
+    from normalization_convolution_blocks_gb300 import api
+    inp = syn.prenorm_block_inputs(N, C, L, d, seed=N + C + L, dtype=dtype)
+    rm_d, rv_d = to(dev, inp.running_mean).clone(), to(dev, inp.running_var).clone()
+    nbt_d = torch.zeros(1, dtype=torch.int64, device=dev)
+    ref = api.prenorm_dilconv_residual_train(to(dev, inp.x), rm_d, rv_d, to(dev, inp.gamma),
+                                             to(dev, inp.beta), inp.eps, 0.1,
+                                             to(dev, inp.weight), to(dev, inp.bias), d,
+                                             num_batches_tracked=nbt_d)
+    rm_h, rv_h = to(dev, inp.running_mean).clone(), to(dev, inp.running_var).clone()
+    nbt_h = torch.zeros(1, dtype=torch.int64, device=dev)
+    pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
+    out = torch.full(tuple(inp.x.shape), float("nan"), dtype=dtype).pin_memory()
+    dt = api.NRC_F32 if dtype == torch.float32 else api.NRC_BF16
+    got = api._train_host(api.load(), dev, dt, pin(inp.x), rm_h, rv_h, pin(inp.gamma),
+                          pin(inp.beta), inp.eps, 0.1, pin(inp.weight), pin(inp.bias), d, None,
+                          3, nbt_h, out, None, None, chunk_n=chunk_n)
+    assert api.query_status() == api.NRC_OK
+    assert torch.equal(got, ref.cpu()), "host entry differs from the device entry"
+    assert torch.equal(rm_h, rm_d) and torch.equal(rv_h, rv_d), "running buffers differ"
+    assert int(nbt_h.item()) == int(nbt_d.item()) == 1
