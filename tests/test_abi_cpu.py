@@ -287,3 +287,89 @@ def test_noalloc_validation_order(lib, kw, expect):
     """The allocation-free entry rejects bad arguments with the workspace entry
     point's codes, then sizes beyond its array, before any CUDA call."""
     assert _noalloc(lib, **kw) == expect
+
+
+def _lin_host(lib, **kw):
+    a = dict(x=FAKE, out=FAKE2, B=8, IN=16, OUT=300, w=FAKE, lb=None, g=None, b=None, rm=FAKE,
+             rv=FAKE, nbt=None, eps=1e-5, m=0.1, tr=1, ab=FAKE, div=1.0, chunk=128, ws=WS,
+             wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.nrc_linear_bn_swish_host(a["x"], a["out"], a["B"], a["IN"], a["OUT"], a["w"],
+                                        a["lb"], a["g"], a["b"], a["rm"], a["rv"], a["nbt"],
+                                        a["eps"], a["m"], a["tr"], a["ab"], a["div"], a["chunk"],
+                                        a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), 1), (dict(ab=None), 1), (dict(rm=None), 1), (dict(g=FAKE), 1),
+    (dict(div=0.0), 1), (dict(m=1.5), 1), (dict(tr=2), 1), (dict(B=1), 2), (dict(chunk=0), 1),
+    (dict(ws=ctypes.c_void_p(0x30000010)), 3), (dict(wsb=8), 4),
+])
+def test_linear_host_validation(lib, kw, expect):
+    """The Linear's host-buffer entry rejects bad arguments before any CUDA call."""
+    assert _lin_host(lib, **kw) == expect
+
+
+def test_linear_host_workspace_query(lib):
+    f = lib.nrc_linear_bn_swish_host_workspace_size
+    B, IN, OUT = 1024, 8192, 8192
+    a, b = f(B, IN, OUT, 1024), f(B, IN, OUT, 2048)
+    # two weight-row and two output chunk buffers grow with the chunk
+    assert b - a >= 2 * 1024 * IN * 4 + 2 * B * 1024 * 4
+    assert f(B, IN, OUT, 100) == f(B, IN, OUT, 128)             # whole 128-feature tiles
+    assert f(B, IN, OUT, 1 << 20) == f(B, IN, OUT, OUT)          # at most out_f
+    assert f(0, IN, OUT, 128) == 0 and f(B, IN, OUT, 0) == 0
+
+
+def _gn_host(lib, **kw):
+    a = dict(x=FAKE, out=FAKE2, N=4, Cin=16, Cout=32, T=64, k=3, s=1, p=1, d=1, w=FAKE,
+             bias=None, G=4, g=FAKE, b=FAKE, eps=1e-5, chunk=2, ws=WS, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.nrc_conv1d_groupnorm_host(a["x"], a["out"], a["N"], a["Cin"], a["Cout"], a["T"],
+                                         a["k"], a["s"], a["p"], a["d"], a["w"], a["bias"],
+                                         a["G"], a["g"], a["b"], a["eps"], a["chunk"], a["ws"],
+                                         a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), 1), (dict(w=None), 1), (dict(G=5), 1), (dict(g=None), 1), (dict(chunk=0), 1),
+    (dict(T=2, k=9, p=0), 1),                                  # the kernel does not fit
+    (dict(k=65, p=40), 2),                                     # more taps than supported
+    (dict(ws=ctypes.c_void_p(0x30000004)), 3), (dict(ws=ctypes.c_void_p(0x30000010)), 3),
+    (dict(wsb=64), 4),
+])
+def test_groupnorm_host_validation(lib, kw, expect):
+    """The GroupNorm host-buffer entry rejects bad arguments before any CUDA call."""
+    assert _gn_host(lib, **kw) == expect
+
+
+def _train_host(lib, **kw):
+    a = dict(x=FAKE, out=FAKE2, dt=0, N=4, C=32, L=64, k=3, d=4, pad=4, rm=FAKE, rv=FAKE,
+             nbt=None, g=FAKE, b=FAKE, eps=1e-5, m=0.1, w=FAKE, bias=FAKE, chunk=2, ws=WS,
+             wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.nrc_prenorm_dilconv_residual_train_host(
+        a["x"], a["out"], a["dt"], a["N"], a["C"], a["L"], a["k"], a["d"], a["pad"], a["rm"],
+        a["rv"], a["nbt"], a["g"], a["b"], a["eps"], a["m"], a["w"], a["bias"], a["chunk"],
+        a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), 1), (dict(g=None), 1), (dict(w=None), 1), (dict(chunk=0), 1),
+    (dict(dt=7), 1), (dict(N=1, L=1), 1), (dict(k=5), 2), (dict(pad=3), 2),
+    (dict(ws=ctypes.c_void_p(0x30000004)), 3), (dict(ws=ctypes.c_void_p(0x30000010)), 3),
+    (dict(wsb=4096), 4),
+])
+def test_train_host_validation(lib, kw, expect):
+    """The training-mode host-buffer entry rejects bad arguments before any CUDA call."""
+    assert _train_host(lib, **kw) == expect
+
+
+def test_train_host_workspace_query(lib):
+    f = lib.nrc_prenorm_dilconv_residual_train_host_workspace_size
+    dev = lib.nrc_prenorm_dilconv_residual_train_workspace_size(32, 256, 4096, 0)
+    one, four = f(32, 256, 4096, 0, 1), f(32, 256, 4096, 0, 4)
+    sample = 256 * 4096 * 4
+    assert one >= dev + 32 * sample + 2 * sample               # device copy of x, out buffers
+    assert four - one == 2 * 3 * sample                          # two out chunk buffers grow
+    assert f(0, 256, 4096, 0, 4) == 0 and f(32, 256, 4096, 0, 0) == 0
