@@ -182,7 +182,7 @@ class ClockSampler:
                 pass
             self.proc = subprocess.Popen(
                 ["nvidia-smi", *sel, f"--query-gpu={CLOCK_FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
