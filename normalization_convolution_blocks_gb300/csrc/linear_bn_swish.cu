@@ -589,7 +589,6 @@ extern "C" nrc_status nrc_linear_bn_swish_host(
     const int F = std::min(out_f, chunk_t * kBM);
     const LinearHostLayout hl = linear_host_layout(B, in_f, out_f, F);
     if (workspace_bytes < hl.total) return NRC_ERR_WORKSPACE;
-    if ((long long)tiles * kBM * in_f >= (1LL << 40)) return NRC_ERR_UNSUPPORTED;
 
     std::lock_guard<std::mutex> lk(g_lin_host_mu);   // the per-device pipe is shared
     LinearHostPipe* hp = nullptr;
