@@ -51,8 +51,8 @@ L2_FLUSH_BYTES = 256 << 20
 # headers) hash to the recorded value, else the line reports null.
 NCU_TRAFFIC = {
     "prenorm_block_f32": {"bytes": 135219200 + 86754048, "src_hash": "2d03b6983ae13010"},
-    "linear_bn_swish_f32": {"bytes": 335566336 + 23069184, "src_hash": "c59fe7baa9fc2bfd"},
-    "linear_bn_swish_eval_f32": {"bytes": 335696128 + 22748928, "src_hash": "c59fe7baa9fc2bfd"},
+    "linear_bn_swish_f32": {"bytes": 335566336 + 23069184, "src_hash": "4154b4a9fd0a1a11"},
+    "linear_bn_swish_eval_f32": {"bytes": 335696128 + 22748928, "src_hash": "4154b4a9fd0a1a11"},
     "prenorm_block_train_f32": {"bytes": 135193856 + 86392320, "src_hash": "2d03b6983ae13010"},
     "conv1d_groupnorm_f32": {"bytes": 8897792 + 0, "src_hash": "2d03b6983ae13010"},
     "prenorm_block_bf16_C256_d1": {"bytes": 67612672 + 22260992, "src_hash": "2d03b6983ae13010"},
