@@ -191,30 +191,41 @@ def test_host_buffer_entry_pageable_input():
     assert np.array_equal(_host_call(inp, 2, pinned=False), _gpu(dev, inp))
 
 
-@pytest.mark.parametrize("which", ["out", "x"])
-def test_bf16_views_at_odd_offsets(which):
-    """x or out starting 2 bytes past an 8-byte boundary: the staged bf16 path
-    (16-byte TMA boxes of x, 8-byte residual/output words) must not be taken,
-    and the result must still match the oracle."""
+@pytest.mark.parametrize("dtype,which,offset", [
+    (torch.bfloat16, "out", 1),     # out 2 bytes past a 16-byte boundary
+    (torch.bfloat16, "out", 4),     # out 8-byte aligned, not 16
+    (torch.bfloat16, "x", 1),
+    (torch.float32, "out", 1),      # out 4 bytes past a 16-byte boundary
+    (torch.float32, "x", 1),
+])
+def test_views_at_unaligned_offsets(dtype, which, offset):
+    """x or out starting past a 16-byte boundary.  x there rules out the TMA
+    boxes of the staged kernel (its rows load into registers instead).  bf16
+    out off an 8-byte boundary rules out the staged kernel's 8-byte residual
+    and output words (the register path runs); 8-byte aligned bf16 out and
+    any fp32 out keep the staged kernel.  Every case must match the oracle
+    and leave everything outside out unchanged."""
     dev = need_gpu()
     from normalization_convolution_blocks_gb300 import api
-    inp = syn.prenorm_block_inputs(2, 64, 256, 4, seed=17, dtype=torch.bfloat16)
+    inp = syn.prenorm_block_inputs(2, 64, 256, 4, seed=17, dtype=dtype)
     n = inp.x.numel()
     x = to(dev, inp.x)
-    g = Guarded(tuple(inp.x.shape), torch.bfloat16, dev, offset=1 if which == "out" else 0)
+    g = Guarded(tuple(inp.x.shape), dtype, dev, offset=offset if which == "out" else 0)
     out = g.view
     if which == "x":
-        xb = torch.empty(n + 1, dtype=torch.bfloat16, device=dev)
-        xb[1:].copy_(x.reshape(-1))
-        x = xb[1:].view(inp.x.shape)
-    assert (x if which == "x" else out).data_ptr() % 8 == 2
+        xb = torch.empty(n + offset, dtype=dtype, device=dev)
+        xb[offset:].copy_(x.reshape(-1))
+        x = xb[offset:].view(inp.x.shape)
+    es = torch.tensor([], dtype=dtype).element_size()
+    assert (x if which == "x" else out).data_ptr() % 16 == offset * es
     got = api.prenorm_dilconv_residual(x, to(dev, inp.running_mean), to(dev, inp.running_var),
                                        to(dev, inp.gamma), to(dev, inp.beta), inp.eps,
                                        to(dev, inp.weight), to(dev, inp.bias), inp.dilation,
                                        out=out)
     assert api.query_status() == api.NRC_OK
-    g.check(f"bf16 {which} at +2 bytes")
-    assert_bf16(got.double().cpu().numpy(), _oracle(inp), f"bf16 {which} at +2 bytes")
+    g.check(f"{dtype} {which} at +{offset * es} bytes")
+    check = assert_f32 if dtype == torch.float32 else assert_bf16
+    check(got.double().cpu().numpy(), _oracle(inp), f"{dtype} {which} at +{offset * es} bytes")
 
 
 @pytest.mark.parametrize("N,C,L,d", [
