@@ -13,7 +13,10 @@ buffers (host->device copies of every input and the device->host copy of the
 output inside the timed region).  L2 is flushed (256 MB write, untimed)
 between timed steps.  The K timed steps run twice: untraced for `value` (as a
 caller runs the library), then with the library's launch trace on for the
-dominant kernel's CUDA-event duration (`roofline`).  Multi-GPU (torchrun) runs independent replicas: the
+dominant kernel's CUDA-event duration (`roofline`).  `graph` reports the same
+call captured once in a CUDA graph and replayed: device time per replay (L2
+flushed between replays) and the host's enqueue cost per call, eager against
+replay.  Multi-GPU (torchrun) runs independent replicas: the
 blocks have no exchange step, so the work is weak-scaled with no collective
 on the data path; the barrier and the max-over-ranks timing use the process
 group only around the timed region.
@@ -519,7 +522,52 @@ def gpu_arm(args, world, rank, local):
     result["e2e"] = dict(value=world * info["flops"] / e2e_s / 1e12, unit="TFLOP/s",
                          h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                          ms_per_step=e2e_s * 1e3, steps=n_e2e)
+    result["graph"] = graph_leg(call, flush, stream, min(steps, 200))
     return result
+
+
+def graph_leg(call, flush, stream, n):
+    """The device-buffer call captured once in a CUDA graph (after a warm-up
+    call on a side stream) and replayed n times: device ms per replay (CUDA
+    events, L2 flushed between replays) and the host's enqueue cost per call,
+    eager calls against replays, each over back-to-back calls (no flush)."""
+    import torch
+    from normalization_convolution_blocks_gb300 import api
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        call()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        starts[i].record(stream)
+        graph.replay()
+        ends[i].record(stream)
+        flush.fill_(1.0)
+    torch.cuda.synchronize()
+    replay_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    m = 50
+    host = {}
+    for kind, fn in (("eager", call), ("graph", graph.replay)):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(m):
+            fn()
+        host[kind] = (time.perf_counter() - t0) / m * 1e6
+        torch.cuda.synchronize()
+    if api.query_status() != api.NRC_OK:
+        raise RuntimeError("device status error in the graph replays")
+    return dict(ms_per_call_median=round(statistics.median(replay_ms), 5),
+                ms_per_call_p10=round(sorted(replay_ms)[n // 10], 5), replays=n,
+                host_us_per_call_eager=round(host["eager"], 1),
+                host_us_per_call_graph=round(host["graph"], 1))
 
 
 # ---------------------------------------------------------------------------
@@ -673,7 +721,7 @@ def main():
                                 else "3 bf16 tensor products per term (hi/lo split), "
                                      "fp32 accumulate")),
         roofline=r["roofline"], e2e=r["e2e"], gpu_launches=r["launches"],
-        clocks=r["clocks"],
+        clocks=r["clocks"], graph=r["graph"],
         ms_per_call_median=round(r["step_ms_median"], 5),
         ms_per_call_p10=round(r["step_ms_p10"], 5), ms_per_call_p90=round(r["step_ms_p90"], 5),
         kernels=r["kernels"],

@@ -75,7 +75,9 @@ def test_json_line_assembly_with_a_stubbed_gpu_arm(monkeypatch, capsys):
                 kernels={}, clocks=dict(sm_mhz=2070.0, sm_max_mhz=2070.0, reasons=[]),
                 info=info, step_ms_p10=0.119, step_ms_p90=0.121, step_ms_median=0.12,
                 e2e=dict(value=50.0, unit="TFLOP/s", h2d_bytes_per_step=1,
-                         d2h_bytes_per_step=1))
+                         d2h_bytes_per_step=1),
+                graph=dict(ms_per_call_median=0.118, ms_per_call_p10=0.117, replays=100,
+                           host_us_per_call_eager=30.0, host_us_per_call_graph=4.0))
     monkeypatch.setattr(bench, "gpu_arm", lambda args, world, rank, local: fake)
     monkeypatch.setattr(sys, "argv", ["bench.py", "--no-cpu-baseline", "--steps", "100"])
     for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
@@ -85,7 +87,7 @@ def test_json_line_assembly_with_a_stubbed_gpu_arm(monkeypatch, capsys):
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "e2e", "gpu_launches", "clocks", "bandwidth",
-                "ms_per_call_median"):
+                "ms_per_call_median", "graph"):
         assert key in line, key
     assert line["n_gpus"] == 1 and line["value"] == 430.0 and line["warmup"] >= 3
     assert line["config"]["workload"] == "prenorm_block_f32"
