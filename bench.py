@@ -160,6 +160,34 @@ def roofline_peaks(info, peaks):
     return bf16 * TF32_PER_BF16, "tf32 = measured bf16 burst x nominal 1.1/2.25"
 
 
+def roofline_of(info, main_ms, peaks):
+    """The dominant kernel's roofline: whichever of the tensor and HBM bounds
+    is longer for the workload, the kernel's achieved rate against it, and the
+    effective fraction (fp32: the three TF32 products per term that 3xTF32
+    compensation issues)."""
+    tensor_peak, tensor_note = roofline_peaks(info, peaks)
+    hbm_peak = peaks["hbm_gbs"]
+    t_tensor = info["flops"] / (tensor_peak * 1e12)
+    t_hbm = info["min_bytes"] / (hbm_peak * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = info["flops"] / (main_ms * 1e-3) / 1e12
+        roof = dict(bound="tensor", achieved=round(achieved, 2), peak=round(tensor_peak, 1),
+                    unit="TFLOP/s", frac=round(achieved / tensor_peak, 4))
+    else:
+        achieved = info["min_bytes"] / (main_ms * 1e-3) / 1e9
+        roof = dict(bound="hbm", achieved=round(achieved, 1), peak=round(hbm_peak, 1),
+                    unit="GB/s", frac=round(achieved / hbm_peak, 4))
+    roof["roofline_ms"] = round(max(t_tensor, t_hbm) * 1e3, 5)
+    if info["dtype"] == "f32" and roof["bound"] == "tensor":
+        t_eff = max(3 * t_tensor, t_hbm)
+        roof["roofline_ms_effective"] = round(t_eff * 1e3, 5)
+        roof["frac_effective"] = round(t_eff / (main_ms * 1e-3), 4)
+    else:
+        roof["roofline_ms_effective"] = roof["roofline_ms"]
+        roof["frac_effective"] = roof["frac"]
+    return roof, tensor_note
+
+
 # ---------------------------------------------------------------------------
 # Clock sampling during the timed region
 # ---------------------------------------------------------------------------
@@ -454,35 +482,14 @@ def gpu_arm(args, world, rank, local):
     ms_per_step = total_ms / steps
     value = whole_job_tflops(world, info["flops"], ms_per_step)
     peaks, peaks_src = load_peaks()
-    tensor_peak, tensor_note = roofline_peaks(info, peaks)
     hbm_peak = peaks["hbm_gbs"]
-    t_tensor = info["flops"] / (tensor_peak * 1e12)
-    t_hbm = info["min_bytes"] / (hbm_peak * 1e9)
-    if t_tensor >= t_hbm:
-        achieved = info["flops"] / (main_ms * 1e-3) / 1e12
-        roof = dict(bound="tensor", achieved=round(achieved, 2), peak=round(tensor_peak, 1),
-                    unit="TFLOP/s", frac=round(achieved / tensor_peak, 4))
-    else:
-        achieved = info["min_bytes"] / (main_ms * 1e-3) / 1e9
-        roof = dict(bound="hbm", achieved=round(achieved, 1), peak=round(hbm_peak, 1),
-                    unit="GB/s", frac=round(achieved / hbm_peak, 4))
+    roof, tensor_note = roofline_of(info, main_ms, peaks)
     tr = NCU_TRAFFIC.get(args.workload)
     roof["traffic"] = (tr["bytes"] if tr and tr["src_hash"] == kernel_source_hash(args.workload)
                        else None)
     roof["kernel"] = main
     roof["kernel_ms"] = round(main_ms, 5)
     roof["peak_source"] = f"{peaks_src}: {tensor_note if roof['bound'] == 'tensor' else 'hbm_gbs'}"
-    roof["roofline_ms"] = round(max(t_tensor, t_hbm) * 1e3, 5)
-    if info["dtype"] == "f32" and roof["bound"] == "tensor":
-        # the effective roofline counts the three TF32 products per term that
-        # 3xTF32-compensated fp32 issues (its fp32-accurate peak is the TF32
-        # peak / 3); it exceeds 1 when the kernel's own compensation costs less
-        t_eff = max(3 * t_tensor, t_hbm)
-        roof["roofline_ms_effective"] = round(t_eff * 1e3, 5)
-        roof["frac_effective"] = round(t_eff / (main_ms * 1e-3), 4)
-    else:
-        roof["roofline_ms_effective"] = roof["roofline_ms"]
-        roof["frac_effective"] = roof["frac"]
     if info["dtype"] == "f32":
         # executed work: three bf16 products per term, against the bf16 peak
         roof["executed_bf16_frac"] = round(3 * info["flops"] / (main_ms * 1e-3) / 1e12
@@ -523,7 +530,67 @@ def gpu_arm(args, world, rank, local):
                          h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                          ms_per_step=e2e_s * 1e3, steps=n_e2e)
     result["graph"] = graph_leg(call, flush, stream, min(steps, 200))
+    if world == 1 and not args.no_other_workloads:
+        del call
+        torch.cuda.empty_cache()
+        result["workloads"] = other_workloads(args.workload, dev, flush, stream, peaks)
     return result
+
+
+def other_workloads(skip, dev, flush, stream, peaks, steps=30):
+    """Every other workload of the library, measured the same way as the
+    headline one but briefly: 3 warm-up calls, then `steps` timed calls
+    untraced (ms/call, median) and `steps` traced (the dominant kernel's
+    CUDA-event time and its roofline fraction), L2 flushed between calls.
+    One clock record covers the whole pass."""
+    import torch
+
+    from normalization_convolution_blocks_gb300 import api
+    from normalization_convolution_blocks_gb300 import synthetic as syn
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    sampler.mark("begin")
+    res = {}
+    for name in syn.WORKLOADS:
+        if name == skip:
+            continue
+        info = workload_info(name)
+        call, _, _ = make_call(name, dev)
+        for _ in range(3):
+            call()
+            flush.fill_(1.0)
+        torch.cuda.synchronize()
+        times = {}
+        for traced in (False, True):
+            starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            api.trace_enable(traced)
+            for i in range(steps):
+                starts[i].record(stream)
+                call()
+                ends[i].record(stream)
+                flush.fill_(1.0)
+            torch.cuda.synchronize()
+            api.trace_enable(False)
+            times[traced] = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        if api.query_status() != api.NRC_OK:
+            raise RuntimeError(f"device status error in workload {name}")
+        main = info["main_kernel"]
+        main_ms = statistics.mean(ms for n, ms in api.trace_records() if n == main)
+        roof, _ = roofline_of(info, main_ms, peaks)
+        med = statistics.median(times[False])
+        res[name] = dict(ms_per_call_median=round(med, 5),
+                         tflops=round(info["flops"] / (med * 1e-3) / 1e12, 2),
+                         kernel=main, kernel_ms=round(main_ms, 5), bound=roof["bound"],
+                         frac=roof["frac"], frac_effective=roof["frac_effective"])
+        del call
+        torch.cuda.empty_cache()
+    sampler.mark("end")
+    res["clocks"] = sampler.stop()
+    res["note"] = (f"{steps} untraced and {steps} traced calls each after 3 warm-up calls, "
+                   "L2 flushed between calls; frac as in roofline")
+    return res
 
 
 def graph_leg(call, flush, stream, n):
@@ -695,6 +762,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the brief pass over the library's other workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -730,6 +799,8 @@ def main():
                        note="the call's algorithmic bytes (inputs read once, output written "
                             "once) over its untraced time"),
     )
+    if "workloads" in r:
+        line["workloads"] = r["workloads"]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     print(json.dumps(line), flush=True)

@@ -92,3 +92,20 @@ def test_json_line_assembly_with_a_stubbed_gpu_arm(monkeypatch, capsys):
     assert line["n_gpus"] == 1 and line["value"] == 430.0 and line["warmup"] >= 3
     assert line["config"]["workload"] == "prenorm_block_f32"
     assert line["bandwidth"]["value"] == pytest.approx(info["min_bytes"] / 0.12e-3 / 1e9, abs=0.1)
+
+
+def test_roofline_of_picks_the_longer_bound_and_scales_the_fraction():
+    """Tensor-bound fp32 workload: strict fraction against the TF32 peak, and
+    the effective one against three TF32 products per term; an HBM-bound one
+    against the copy bandwidth, with effective = strict."""
+    peaks = dict(bf16_tflops=2250.0, hbm_gbs=8000.0)
+    tf32 = 2250.0 * bench.TF32_PER_BF16
+    f32 = dict(flops=1e12, min_bytes=1e6, dtype="f32")
+    ms = 2.0 * 1e12 / (tf32 * 1e12) * 1e3          # twice the strict roofline time
+    roof, _ = bench.roofline_of(f32, ms, peaks)
+    assert roof["bound"] == "tensor" and roof["frac"] == pytest.approx(0.5, abs=1e-4)
+    assert roof["frac_effective"] == pytest.approx(1.5, abs=1e-4)
+    hbm = dict(flops=1e6, min_bytes=8e9, dtype="bf16")
+    roof, _ = bench.roofline_of(hbm, 4.0, peaks)      # 8 GB at 8 TB/s is 1 ms
+    assert roof["bound"] == "hbm" and roof["frac"] == pytest.approx(0.25, abs=1e-4)
+    assert roof["frac_effective"] == roof["frac"]
