@@ -533,8 +533,48 @@ def gpu_arm(args, world, rank, local):
     if world == 1 and not args.no_other_workloads:
         del call
         torch.cuda.empty_cache()
-        result["workloads"] = other_workloads(args.workload, dev, flush, stream, peaks)
+        try:
+            result["workloads"] = other_workloads(args.workload, dev, flush, stream, peaks)
+        except Exception as e:
+            result["workloads"] = dict(error=f"{type(e).__name__}: {e}"[:200])
     return result
+
+
+def measure_briefly(name, dev, flush, stream, peaks, steps):
+    """One workload: 3 warm-up calls, `steps` untraced calls (median ms) and
+    `steps` traced calls (the dominant kernel's mean CUDA-event ms)."""
+    import torch
+
+    from normalization_convolution_blocks_gb300 import api
+    info = workload_info(name)
+    call, _, _ = make_call(name, dev)
+    for _ in range(3):
+        call()
+        flush.fill_(1.0)
+    torch.cuda.synchronize()
+    times = {}
+    for traced in (False, True):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        api.trace_enable(traced)
+        for i in range(steps):
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+            flush.fill_(1.0)
+        torch.cuda.synchronize()
+        api.trace_enable(False)
+        times[traced] = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    if api.query_status() != api.NRC_OK:
+        raise RuntimeError("device status error")
+    main = info["main_kernel"]
+    main_ms = statistics.mean(ms for n, ms in api.trace_records() if n == main)
+    roof, _ = roofline_of(info, main_ms, peaks)
+    med = statistics.median(times[False])
+    return dict(ms_per_call_median=round(med, 5),
+                tflops=round(info["flops"] / (med * 1e-3) / 1e12, 2),
+                kernel=main, kernel_ms=round(main_ms, 5), bound=roof["bound"],
+                frac=roof["frac"], frac_effective=roof["frac_effective"])
 
 
 def other_workloads(skip, dev, flush, stream, peaks, steps=30):
@@ -555,36 +595,15 @@ def other_workloads(skip, dev, flush, stream, peaks, steps=30):
     for name in syn.WORKLOADS:
         if name == skip:
             continue
-        info = workload_info(name)
-        call, _, _ = make_call(name, dev)
-        for _ in range(3):
-            call()
-            flush.fill_(1.0)
-        torch.cuda.synchronize()
-        times = {}
-        for traced in (False, True):
-            starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-            ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-            api.trace_enable(traced)
-            for i in range(steps):
-                starts[i].record(stream)
-                call()
-                ends[i].record(stream)
-                flush.fill_(1.0)
-            torch.cuda.synchronize()
-            api.trace_enable(False)
-            times[traced] = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-        if api.query_status() != api.NRC_OK:
-            raise RuntimeError(f"device status error in workload {name}")
-        main = info["main_kernel"]
-        main_ms = statistics.mean(ms for n, ms in api.trace_records() if n == main)
-        roof, _ = roofline_of(info, main_ms, peaks)
-        med = statistics.median(times[False])
-        res[name] = dict(ms_per_call_median=round(med, 5),
-                         tflops=round(info["flops"] / (med * 1e-3) / 1e12, 2),
-                         kernel=main, kernel_ms=round(main_ms, 5), bound=roof["bound"],
-                         frac=roof["frac"], frac_effective=roof["frac_effective"])
-        del call
+        try:
+            res[name] = measure_briefly(name, dev, flush, stream, peaks, steps)
+        except Exception as e:      # a secondary figure must not cost the headline line
+            res[name] = dict(error=f"{type(e).__name__}: {e}"[:200])
+            try:
+                torch.cuda.synchronize()
+                api.query_status()  # reads and clears the device status word
+            except Exception:
+                break
         torch.cuda.empty_cache()
     sampler.mark("end")
     res["clocks"] = sampler.stop()
