@@ -29,6 +29,12 @@
  *   is the legacy default stream).  No call synchronises the host.  The
  *   workspace and outputs must not be reused until the stream has passed the
  *   call.
+ * - Stream capture: the device-buffer entry points enqueue only memsets and
+ *   kernel launches on `stream`, so a call can be captured into a CUDA graph
+ *   and replayed.  A replay gives the same result as the call, bit for bit.
+ *   Make the first call on a device outside capture: it sets the kernels'
+ *   shared-memory limit and looks up the library's device symbols.  The
+ *   host-buffer entries (*_host) use library streams and are not capturable.
  * - Argument errors are reported by the return value before anything is
  *   launched; a failed launch returns NRC_ERR_CUDA.  A device-side wait that
  *   gives up (see nrc_set_wait_timeout_ns) is recorded in the device status
