@@ -32,9 +32,17 @@ def _ref(g, G, bias=None, affine=True, stride=1, padding=1, dilation=1):
 
 
 def test_full_workload():
+    """Every element, and each sample's groups on their own (an error in one
+    sample's statistics cannot hide in the global norm)."""
     dev = need_gpu()
     g = syn.WORKLOADS["conv1d_groupnorm_f32"].make(seed=0)
-    assert_f32(_gpu(dev, g, 32), _ref(g, 32), "N16 128->256 T1024 G32")
+    got, ref = _gpu(dev, g, 32), _ref(g, 32)
+    assert_f32(got, ref, "N16 128->256 T1024 G32")
+    cpg = got.shape[1] // 32
+    for n in range(got.shape[0]):
+        for grp in range(32):
+            sl = slice(grp * cpg, (grp + 1) * cpg)
+            assert_f32(got[n, sl], ref[n, sl], f"sample {n} group {grp}")
 
 
 @pytest.mark.parametrize("N,Cin,Cout,T,G", [
