@@ -150,3 +150,57 @@ def test_block_train_graph_replay():
                                                       workspace=ws)
     x2 = to(dev, syn.prenorm_block_inputs(N, C, L, d, seed=4).x)
     _replay_matches(call, out, [x], [x2], state=(rm, rv, nbt))
+
+
+@pytest.mark.gpu
+def test_chained_entries_in_one_graph():
+    """The block, then conv + GroupNorm on its output, then the Linear on a
+    reshaped slice of that, captured as one graph: a replay equals the three
+    calls run eagerly, also after new x values are copied in."""
+    dev = need_gpu()
+    from normalization_convolution_blocks_gb300 import api
+    N, C, L, d, G, OUT = 4, 64, 512, 8, 8, 96
+    inp = syn.prenorm_block_inputs(N, C, L, d, seed=21)
+    x, rm, rv, g, b, w, bias = (to(dev, t) for t in (inp.x, inp.running_mean, inp.running_var,
+                                                     inp.gamma, inp.beta, inp.weight, inp.bias))
+    gn = syn.conv_groupnorm_inputs(N, C, C, L, G, seed=22)
+    gw, gg, gb = (to(dev, t) for t in (gn.weight, gn.gamma, gn.beta))
+    li = syn.linear_bn_swish_inputs(N * C, L, OUT, seed=23, random_affine=True)
+    lw, lb, lg, lbe, lab = (to(dev, t) for t in (li.weight, li.lin_bias, li.gamma, li.beta,
+                                                 li.add_bias))
+    lrm = torch.zeros(OUT, device=dev)
+    lrv = torch.ones(OUT, device=dev)
+    y1 = torch.empty_like(x)
+    y2 = torch.empty_like(x)
+    y3 = torch.empty(N * C, OUT, device=dev)
+    ws1 = torch.empty(api.prenorm_dilconv_residual_workspace_size(C), dtype=torch.uint8,
+                      device=dev)
+    ws2 = torch.empty(api.conv1d_groupnorm_workspace_size(N, C, C, L, G), dtype=torch.uint8,
+                      device=dev)
+    ws3 = torch.empty(api.linear_bn_swish_workspace_size(N * C, L, OUT), dtype=torch.uint8,
+                      device=dev)
+
+    def chain():
+        api.prenorm_dilconv_residual(x, rm, rv, g, b, inp.eps, w, bias, d, out=y1, workspace=ws1)
+        api.conv1d_groupnorm(y1, gw, None, G, gg, gb, gn.eps, out=y2, workspace=ws2)
+        api.linear_bn_swish(y2.view(N * C, L), lw, lb, lg, lbe, lrm, lrv, lab, 2.0, li.eps,
+                            li.momentum, training=False, out=y3, workspace=ws3)
+
+    x2 = to(dev, syn.prenorm_block_inputs(N, C, L, d, seed=24).x)
+    x1 = x.clone()
+    want = []
+    for xv in (x1, x2):
+        x.copy_(xv)
+        chain()
+        torch.cuda.synchronize()
+        want.append((y1.clone(), y2.clone(), y3.clone()))
+    x.copy_(x1)
+    graph = _capture(chain)
+    for xv, (w1, w2, w3) in zip((x1, x2), want):
+        x.copy_(xv)
+        for t in (y1, y2, y3):
+            t.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y1, w1) and torch.equal(y2, w2) and torch.equal(y3, w3)
+    _status_ok()
