@@ -615,8 +615,9 @@ def other_workloads(skip, dev, flush, stream, peaks, steps=30):
 def graph_leg(call, flush, stream, n):
     """The device-buffer call captured once in a CUDA graph (after a warm-up
     call on a side stream) and replayed n times: device ms per replay (CUDA
-    events, L2 flushed between replays) and the host's enqueue cost per call,
-    eager calls against replays, each over back-to-back calls (no flush)."""
+    events, L2 flushed between replays); then, over 50 back-to-back calls (no
+    flush), the host's enqueue cost per call and the wall time per call until
+    the GPU has finished, eager calls against replays."""
     import torch
     from normalization_convolution_blocks_gb300 import api
     side = torch.cuda.Stream()
@@ -639,7 +640,7 @@ def graph_leg(call, flush, stream, n):
     torch.cuda.synchronize()
     replay_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     m = 50
-    host = {}
+    host, wall = {}, {}
     for kind, fn in (("eager", call), ("graph", graph.replay)):
         fn()
         torch.cuda.synchronize()
@@ -648,12 +649,15 @@ def graph_leg(call, flush, stream, n):
             fn()
         host[kind] = (time.perf_counter() - t0) / m * 1e6
         torch.cuda.synchronize()
+        wall[kind] = (time.perf_counter() - t0) / m * 1e6
     if api.query_status() != api.NRC_OK:
         raise RuntimeError("device status error in the graph replays")
     return dict(ms_per_call_median=round(statistics.median(replay_ms), 5),
                 ms_per_call_p10=round(sorted(replay_ms)[n // 10], 5), replays=n,
                 host_us_per_call_eager=round(host["eager"], 1),
-                host_us_per_call_graph=round(host["graph"], 1))
+                host_us_per_call_graph=round(host["graph"], 1),
+                back_to_back_us_per_call_eager=round(wall["eager"], 1),
+                back_to_back_us_per_call_graph=round(wall["graph"], 1))
 
 
 # ---------------------------------------------------------------------------
