@@ -260,3 +260,30 @@ def test_back_to_back_calls_with_alternating_weights(N, C, L, d):
     for i, g in enumerate(guards):
         g.check(f"call {i}")
         assert torch.equal(g.view, ref[i % 2]), f"call {i}"
+
+
+def test_more_than_2_31_elements_sampled_rows():
+    """N=128 C=256 L=65664 in bf16 storage: 2^31 + 4.2 M elements per tensor,
+    so every element offset past 2^31 has to be formed in 64 bits.  Rows of the
+    first, a middle and the last sample are compared with the oracle (run on
+    one sample at a time); the 65,664 tiles also stress the persistent
+    schedule."""
+    dev = need_gpu()
+    from normalization_convolution_blocks_gb300 import api
+    N, C, L, d = 128, 256, 65664, 128
+    assert N * C * L > 2 ** 31
+    inp = syn.prenorm_block_inputs(N, C, L, d, seed=71, dtype=torch.bfloat16)
+    x = to(dev, inp.x)
+    out = torch.empty_like(x)
+    api.prenorm_dilconv_residual(x, to(dev, inp.running_mean), to(dev, inp.running_var),
+                                 to(dev, inp.gamma), to(dev, inp.beta), inp.eps,
+                                 to(dev, inp.weight), to(dev, inp.bias), d, out=out)
+    assert api.query_status() == api.NRC_OK
+    rng = np.random.default_rng(5)
+    for n in (0, 77, N - 1):
+        ro = np.concatenate([[0, C - 1], rng.integers(0, C, 4)])
+        ref = oracle.prenorm_block_rows(inp.x[n:n + 1], inp.running_mean, inp.running_var,
+                                        inp.gamma, inp.beta, inp.eps, inp.weight, inp.bias, d,
+                                        np.zeros(len(ro), dtype=np.int32), ro)
+        got = out[n, torch.as_tensor(ro, device=dev)].double().cpu().numpy()
+        assert_bf16(got, ref, f"sample {n} rows {list(ro)}")
